@@ -1,0 +1,163 @@
+/*
+ * moe_ffn.h -- C ABI of the MoE FFN layer forward for GB300 (sm_103a).
+ *
+ * The layer (one tensor-parallel rank, one GPU):
+ *
+ *   out[t] = sum_j w[t,j] * E_{id[t,j]}(x[t]) + S(x[t])
+ *   E_e(v) = ( SiLU(v . Wg_e^T) * (v . Wu_e^T) ) . Wd_e^T      (routed expert e)
+ *   S(v)   = ( SiLU(v . Wsg^T)  * (v . Wsu^T)  ) . Wsd^T       (shared expert)
+ *
+ * id[t,:] are the k experts with the largest fp32 router logits
+ * l[t,e] = x[t] . Wr[e] + b[e], and w[t,:] is the softmax over those k logits.
+ *
+ * Source of the structure: "Ascend 910C LLM inference optimisation, part 2"
+ * (Dewu Tech), section on MoE multi-stream overlap -- the layer runs the routed
+ * experts (GroupedMatmul), the shared expert and a reduction; the shared
+ * expert's gate_up (part 1) and down (part 2) matmuls read the same hidden
+ * states and do not depend on the routed path, so they run on a side stream
+ * that the default stream waits for; the routed path is dispatch -> gmm1 ->
+ * gmm2 -> combine.  The reduction is the identity at one rank.  The router,
+ * the top-k renormalisation and SiLU*mul follow the layer's definition in the
+ * benchmark shapes (fp32 router, renormalised top-k softmax, bf16 SwiGLU).
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers unless stated otherwise; the caller owns all
+ *    memory, streams and events.  No call allocates device memory.
+ *  - Every call is asynchronous on the given stream and never synchronises
+ *    with the host (moe_last_device_error excepted).
+ *  - bf16 tensors are row-major, 16-byte aligned; K-major weights ([rows][K]).
+ *  - Arguments are checked on the host before anything is launched:
+ *    MOE_ERR_INVALID for null/negative/inconsistent arguments,
+ *    MOE_ERR_UNSUPPORTED for shapes or alignments the kernels do not handle
+ *    (there is no fallback path), MOE_ERR_WORKSPACE for a workspace that is too
+ *    small, MOE_ERR_CUDA if a launch fails.
+ *  - Device-side checks (an expert id out of range, group offsets that are not
+ *    monotone or exceed the stated row bound, a bounded wait that expired)
+ *    skip the offending work and record the first such code in a per-device
+ *    status word read by moe_last_device_error().
+ *  - T == 0 is valid and launches nothing.
+ */
+#ifndef MOE_FFN_H_
+#define MOE_FFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = -1,
+  MOE_ERR_UNSUPPORTED = -2,
+  MOE_ERR_WORKSPACE = -3,
+  MOE_ERR_CUDA = -4,
+  MOE_ERR_TIMEOUT = -5,      /* device: a bounded wait expired */
+  MOE_ERR_DEVICE_CHECK = -6  /* device: an index or offset failed its range check */
+} moe_status;
+
+/* Layer sizes: hidden H, routed experts E, top-k k, expert intermediate I,
+ * shared-expert intermediate I_s (0 = no shared expert). */
+typedef struct {
+  int H, E, k, I, I_s;
+} moe_dims;
+
+/* Layer weights (device pointers, caller-owned).
+ *  w_router    fp32 [E][H]
+ *  router_bias fp32 [E] or NULL; -INFINITY keeps an expert from being chosen
+ *  w_gate_up   bf16 [E][2I][H]: rows 0..I-1 gate, rows I..2I-1 up
+ *  w_down      bf16 [E][H][I]
+ *  ws_gate_up  bf16 [2I_s][H] (NULL iff I_s == 0)
+ *  ws_down     bf16 [H][I_s]  (NULL iff I_s == 0) */
+typedef struct {
+  const float* w_router;
+  const float* router_bias;
+  const void* w_gate_up;
+  const void* w_down;
+  const void* ws_gate_up;
+  const void* ws_down;
+} moe_weights;
+
+/* Router: fp32 logits l[t,e] = sum_h x[t,h]*Wr[e,h] + b[e]; the k largest
+ * (ties to the lower id) become topk_ids[t,:] in ascending id order and
+ * topk_w[t,:] = softmax over those k logits (the full softmax over E
+ * renormalised over the chosen k).
+ *  x        bf16 [T][H];  w_router fp32 [E][H];  bias fp32 [E] or NULL
+ *  topk_ids int32 [T][k] (out);  topk_w fp32 [T][k] (out)
+ *  ws       scratch of moe_route_workspace_bytes(T, E) bytes (256-B aligned)
+ * Supported: 1 <= k <= min(E, 16), E <= 512, H % 8 == 0. */
+MOE_API size_t moe_route_workspace_bytes(int T, int E);
+MOE_API int moe_route(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
+              int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Dispatch (permute): a deterministic counting sort of the T*k (token, slot)
+ * pairs by (expert ascending, token ascending).
+ *  topk_ids       int32 [T][k], distinct ids in [0,E) per token (device-checked)
+ *  expert_offsets int32 [E+1] (out): exclusive prefix sum of per-expert counts
+ *  sorted_token   int32 [T*k] (out): token of permuted row r
+ *  inv_perm       int32 [T*k] (out): permuted row of pair (t,j) at t*k+j
+ *  x, x_perm      bf16 [T][H] in, bf16 [T*k][H] out (x_perm[r] = x[sorted_token[r]]);
+ *                 x_perm may be NULL to skip the row gather (x is then unused)
+ *  ws             scratch of moe_permute_workspace_bytes(T, E) bytes
+ * Bit-exact: the result does not depend on thread scheduling. */
+MOE_API size_t moe_permute_workspace_bytes(int T, int E);
+MOE_API int moe_permute(const int32_t* topk_ids, const void* x, int T, int H, int E, int k, int32_t* expert_offsets,
+                int32_t* sorted_token, int32_t* inv_perm, void* x_perm, void* ws, size_t ws_bytes,
+                cudaStream_t stream);
+
+/* GroupedMatmul (gmm1/gmm2): for each group g, rows r in
+ * [group_offsets[g], group_offsets[g+1]) of A:
+ *   act == 0:  out[r, :] = A[r, :] . W[g]^T                  W bf16 [G][N][K]
+ *   act == 1:  out[r, :] = SiLU(A[r] . Wg^T) * (A[r] . Wu^T)  W bf16 [G][2N][K]
+ *              (rows 0..N-1 of W[g] gate, N..2N-1 up)
+ *  a             bf16 [rows_max][K]
+ *  group_offsets int32 [G+1] on the device (never read by the host); NULL
+ *                means one group covering rows [0, rows_max) (requires G == 1)
+ *  rows_max      host upper bound on group_offsets[G] (device-checked)
+ *  out           bf16 [rows_max][N]; rows outside every group are not written
+ * bf16 inputs, fp32 accumulation in tensor memory, bf16 (round-to-nearest)
+ * output.  Supported: K % 64 == 0, N % 64 == 0, G <= 1024. */
+MOE_API int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max, int N,
+                     int K, int act, void* out, cudaStream_t stream);
+
+/* Combine: out[t] = bf16( sum_j topk_w[t,j] * y[inv_perm[t*k+j]] + shared[t] ),
+ * accumulated in fp32 in slot order j = 0..k-1, then the shared row.
+ *  y bf16 [T*k][H];  inv_perm int32 [T*k];  topk_w fp32 [T][k]
+ *  shared bf16 [T][H] or NULL;  out bf16 [T][H]
+ * Supported: H % 8 == 0, H <= 8192. */
+MOE_API int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const float* topk_w, const void* shared,
+                          int T, int H, int k, void* out, cudaStream_t stream);
+
+/* The whole layer: route -> permute -> gmm1(+SiLU*mul) -> gmm2 on `stream`;
+ * the shared expert's two matmuls on `side` between ev_fork (recorded on
+ * `stream`, waited by `side`) and ev_join (recorded on `side`, waited by
+ * `stream` before the combine).  Exactly one fork and one join event per call.
+ * `side` and the events may be NULL when d->I_s == 0.  ws holds every
+ * intermediate; size it with moe_workspace_bytes(d, T).
+ *  x bf16 [T][H] (device);  out bf16 [T][H] (device) */
+MOE_API size_t moe_workspace_bytes(const moe_dims* d, int T);
+MOE_API int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, void* out, void* ws,
+                size_t ws_bytes, cudaStream_t stream, cudaStream_t side, cudaEvent_t ev_fork,
+                cudaEvent_t ev_join);
+
+/* Reads and clears the current device's status word (first device-side error
+ * since the last read, MOE_OK if none).  Synchronises `stream`. */
+MOE_API int moe_last_device_error(cudaStream_t stream);
+
+/* Number of kernels the last successful call of each entry point launched on
+ * the current host thread (for accounting in benchmarks). */
+MOE_API int moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H_ */

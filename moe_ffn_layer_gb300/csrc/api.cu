@@ -1,0 +1,268 @@
+// C ABI of the MoE FFN layer forward: argument checks, workspace layout and
+// the two-stream orchestration of moe_forward.
+//
+// Orchestration ("Ascend 910C LLM inference optimisation, part 2" (Dewu Tech),
+// section on MoE multi-stream overlap): the shared expert reads the same
+// hidden states as the routed experts and nothing of theirs, so its gate_up
+// and down matmuls run on a side stream, forked from the main stream by one
+// event and joined back by one event just before the combine.  The same page
+// drops the per-step dispatch/combine/gmm2 events once the overlap exists and
+// preallocates events instead of creating them per step: here the caller owns
+// exactly two events and the library creates none.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+__device__ int g_status;   // first device-side error since the last read, per device
+
+thread_local int t_last_launches = 0;
+
+struct DevInfo {
+  int* status = nullptr;
+  int sms = 0;
+  bool init = false;
+};
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+int dev_info(DevInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    d.status = static_cast<int*>(p);
+    d.init = true;
+  }
+  *out = &d;
+  return MOE_OK;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every intermediate of moe_forward, 256-byte aligned, in one caller-owned buffer.
+struct Layout {
+  size_t logits, ids, w, offsets, sorted, inv, pcounts, xperm, h, y, hs, s, total;
+};
+
+Layout layout(const moe_dims* d, int T) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = o;
+    o += moe::align_up(bytes);
+    return r;
+  };
+  const size_t Tk = static_cast<size_t>(T) * d->k;
+  L.logits = take(moe::route_ws_bytes(T, d->E));
+  L.ids = take(Tk * 4);
+  L.w = take(Tk * 4);
+  L.offsets = take((static_cast<size_t>(d->E) + 1) * 4);
+  L.sorted = take(Tk * 4);
+  L.inv = take(Tk * 4);
+  L.pcounts = take(moe::permute_ws_bytes(T, d->E));
+  L.xperm = take(Tk * d->H * 2);
+  L.h = take(Tk * d->I * 2);
+  L.y = take(Tk * d->H * 2);
+  L.hs = take(static_cast<size_t>(T) * d->I_s * 2);
+  L.s = take(static_cast<size_t>(T) * d->H * 2);
+  L.total = o;
+  return L;
+}
+
+int check_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID;
+  if (d->H <= 0 || d->E <= 0 || d->k <= 0 || d->I <= 0 || d->I_s < 0) return MOE_ERR_INVALID;
+  if (d->k > d->E) return MOE_ERR_INVALID;
+  if (d->E > moe::kMaxExperts || d->k > moe::kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (d->H % 64 || d->I % 64 || d->I_s % 64) return MOE_ERR_UNSUPPORTED;
+  if (d->E > moe::grouped_gemm_max_groups()) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_route_workspace_bytes(int T, int E) {
+  if (T < 0 || E <= 0) return 0;
+  return moe::route_ws_bytes(T, E);
+}
+
+int moe_route(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
+              int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  t_last_launches = 0;
+  if (T < 0 || H <= 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID;
+  if (E > moe::kMaxExperts || k > moe::kMaxTopK || H % 8) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !topk_ids || !topk_w || !ws) return MOE_ERR_INVALID;
+  if (!al16(x) || !al16(w_router) || !al16(ws) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_w) & 3u) || (reinterpret_cast<uintptr_t>(bias) & 3u))
+    return MOE_ERR_UNSUPPORTED;
+  if (ws_bytes < moe::route_ws_bytes(T, E)) return MOE_ERR_WORKSPACE;
+  int n = 0;
+  const int rc = moe::route_launch(x, w_router, bias, T, H, E, k, topk_ids, topk_w, static_cast<float*>(ws), stream,
+                                   &n);
+  t_last_launches = n;
+  return rc;
+}
+
+size_t moe_permute_workspace_bytes(int T, int E) {
+  if (T < 0 || E <= 0) return 0;
+  return moe::permute_ws_bytes(T, E);
+}
+
+int moe_permute(const int32_t* topk_ids, const void* x, int T, int H, int E, int k, int32_t* expert_offsets,
+                int32_t* sorted_token, int32_t* inv_perm, void* x_perm, void* ws, size_t ws_bytes,
+                cudaStream_t stream) {
+  t_last_launches = 0;
+  if (T < 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID;
+  if (E > moe::kMaxExperts || static_cast<long long>(T) * k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  if (x_perm && (H <= 0)) return MOE_ERR_INVALID;
+  if (x_perm && H % 8) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !expert_offsets || !sorted_token || !inv_perm) return MOE_ERR_INVALID;
+  if (x_perm && (!x || !al16(x) || !al16(x_perm))) return x ? MOE_ERR_UNSUPPORTED : MOE_ERR_INVALID;
+  const size_t need = moe::permute_ws_bytes(T, E);
+  if (need && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  DevInfo* di = nullptr;
+  int rc = dev_info(&di);
+  if (rc) return rc;
+  int n = 0;
+  rc = moe::permute_launch(topk_ids, x, T, H, E, k, expert_offsets, sorted_token, inv_perm, x_perm,
+                           static_cast<int32_t*>(ws), di->status, di->sms, stream, &n);
+  t_last_launches = n;
+  return rc;
+}
+
+int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max, int N, int K,
+                     int act, void* out, cudaStream_t stream) {
+  t_last_launches = 0;
+  if (G <= 0 || rows_max < 0 || N <= 0 || K <= 0 || (act != 0 && act != 1)) return MOE_ERR_INVALID;
+  if (!group_offsets && G != 1) return MOE_ERR_INVALID;
+  if (G > moe::grouped_gemm_max_groups() || N % 64 || K % 64) return MOE_ERR_UNSUPPORTED;
+  if (rows_max == 0) return MOE_OK;
+  if (!a || !w || !out) return MOE_ERR_INVALID;
+  if (!al16(a) || !al16(w) || !al16(out) || (reinterpret_cast<uintptr_t>(group_offsets) & 3u))
+    return MOE_ERR_UNSUPPORTED;
+  DevInfo* di = nullptr;
+  int rc = dev_info(&di);
+  if (rc) return rc;
+  int n = 0;
+  rc = moe::grouped_gemm_launch(a, w, group_offsets, G, rows_max, N, K, act, out, di->status, di->sms, stream, &n);
+  t_last_launches = n;
+  return rc;
+}
+
+int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const float* topk_w, const void* shared, int T,
+                          int H, int k, void* out, cudaStream_t stream) {
+  t_last_launches = 0;
+  if (T < 0 || H <= 0 || k <= 0) return MOE_ERR_INVALID;
+  if (k > moe::kMaxTopK || H % 8) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y || !inv_perm || !topk_w || !out) return MOE_ERR_INVALID;
+  if (!al16(y) || !al16(out) || (shared && !al16(shared))) return MOE_ERR_UNSUPPORTED;
+  int n = 0;
+  const int rc = moe::combine_launch(y, inv_perm, topk_w, shared, T, H, k, static_cast<long long>(T) * k, out,
+                                     stream, &n);
+  t_last_launches = n;
+  return rc;
+}
+
+size_t moe_workspace_bytes(const moe_dims* d, int T) {
+  if (check_dims(d) != MOE_OK || T < 0) return 0;
+  return layout(d, T).total;
+}
+
+int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, void* out, void* ws,
+                size_t ws_bytes, cudaStream_t stream, cudaStream_t side, cudaEvent_t ev_fork, cudaEvent_t ev_join) {
+  t_last_launches = 0;
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!w || T < 0) return MOE_ERR_INVALID;
+  if (static_cast<long long>(T) * d->k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  const bool has_shared = d->I_s > 0;
+  if (!x || !out || !ws || !w->w_router || !w->w_gate_up || !w->w_down) return MOE_ERR_INVALID;
+  if (has_shared && (!w->ws_gate_up || !w->ws_down || !side || !ev_fork || !ev_join)) return MOE_ERR_INVALID;
+  if (!al16(x) || !al16(out) || !al16(ws) || !al16(w->w_router) || !al16(w->w_gate_up) || !al16(w->w_down) ||
+      (reinterpret_cast<uintptr_t>(w->router_bias) & 3u) ||
+      (has_shared && (!al16(w->ws_gate_up) || !al16(w->ws_down))))
+    return MOE_ERR_UNSUPPORTED;
+  const Layout L = layout(d, T);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  DevInfo* di = nullptr;
+  rc = dev_info(&di);
+  if (rc) return rc;
+
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* logits = reinterpret_cast<float*>(base + L.logits);
+  int32_t* ids = reinterpret_cast<int32_t*>(base + L.ids);
+  float* tw = reinterpret_cast<float*>(base + L.w);
+  int32_t* offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  int32_t* sorted = reinterpret_cast<int32_t*>(base + L.sorted);
+  int32_t* inv = reinterpret_cast<int32_t*>(base + L.inv);
+  int32_t* pcounts = reinterpret_cast<int32_t*>(base + L.pcounts);
+  void* xperm = base + L.xperm;
+  void* h = base + L.h;
+  void* y = base + L.y;
+  void* hs = base + L.hs;
+  void* s = base + L.s;
+  const int rows = T * d->k;
+  int n = 0;
+
+  // shared expert on the side stream, forked from `stream`
+  if (has_shared) {
+    if (cudaEventRecord(ev_fork, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamWaitEvent(side, ev_fork, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    rc = moe::grouped_gemm_launch(x, w->ws_gate_up, nullptr, 1, T, d->I_s, d->H, 1, hs, di->status, di->sms, side,
+                                  &n);
+    if (!rc)
+      rc = moe::grouped_gemm_launch(hs, w->ws_down, nullptr, 1, T, d->H, d->I_s, 0, s, di->status, di->sms, side,
+                                    &n);
+    if (rc) return rc;
+    if (cudaEventRecord(ev_join, side) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // routed path on `stream`: route -> dispatch -> gmm1 (+SiLU*mul) -> gmm2
+  rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, stream, &n);
+  if (!rc)
+    rc = moe::permute_launch(ids, x, T, d->H, d->E, d->k, offsets, sorted, inv, xperm, pcounts, di->status, di->sms,
+                             stream, &n);
+  if (!rc)
+    rc = moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, di->sms,
+                                  stream, &n);
+  if (!rc)
+    rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, di->sms, stream,
+                                  &n);
+  if (rc) return rc;
+  // join, then combine
+  if (has_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  rc = moe::combine_launch(y, inv, tw, has_shared ? s : nullptr, T, d->H, d->k, rows, out, stream, &n);
+  t_last_launches = n;
+  return rc;
+}
+
+int moe_last_device_error(cudaStream_t stream) {
+  DevInfo* di = nullptr;
+  int rc = dev_info(&di);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, di->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  const int zero = 0;
+  if (v != 0 && cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return v;
+}
+
+int moe_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,29 @@
+// Internal launch functions of the MoE FFN library (host side).  Each checks
+// nothing that the C-ABI layer has already checked, returns a moe_status and
+// adds the number of kernels it launched to *launches.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+size_t route_ws_bytes(int T, int E);
+int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
+                 int32_t* topk_ids, float* topk_w, float* logits_ws, cudaStream_t stream, int* launches);
+
+size_t permute_ws_bytes(int T, int E);
+int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, int k, int32_t* offsets,
+                   int32_t* sorted_token, int32_t* inv_perm, void* x_perm, int32_t* block_counts, int* status,
+                   int num_sms, cudaStream_t stream, int* launches);
+
+bool grouped_gemm_weights_on_m(int G, int rows_max, int N);
+int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
+                        int act, void* out, int* status, int grid_cap, cudaStream_t stream, int* launches);
+int grouped_gemm_max_groups();
+
+int combine_launch(const void* y, const int32_t* inv_perm, const float* topk_w, const void* shared, int T, int H,
+                   int k, long long rows_max, void* out, cudaStream_t stream, int* launches);
+
+}  // namespace moe

@@ -1,0 +1,239 @@
+// Dispatch of the MoE FFN layer at one expert-parallel rank: a counting sort of
+// the T*k (token, slot) pairs by (expert ascending, token ascending), the
+// per-expert row offsets of the grouped matmuls, the inverse map used by the
+// combine, and the row gather x_perm[r] = x[sorted_token[r]].
+//
+// "dispatch" is the step before gmm1 on the routed path ("Ascend 910C LLM
+// inference optimisation, part 2" (Dewu Tech), section on MoE multi-stream
+// overlap); its result stays on the device, as the same page's sampling
+// section asks of index work (no device-to-host sync on the path).
+//
+// Determinism: within a block of 256 tokens, the pairs of expert e form a
+// 256-bit mask indexed by token (atomicOr, order-free).  The rank of pair
+// (t, e) among the block's pairs of e is the popcount of the mask bits below
+// t; adding the block's base (an exclusive scan over blocks, then over
+// experts) gives the row.  Nothing depends on thread scheduling.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTB = 256;            // tokens per block (threads per block)
+constexpr int kMaskWords = kTB / 32;
+
+// Validates token t's ids (in [0,E), pairwise distinct) and ORs its bits into
+// the block mask.  Returns false (and records the error) for a bad token.
+__device__ __forceinline__ bool mask_token(const int32_t* ids, int t, int tl, int E, int k, uint32_t* mask,
+                                           int* status) {
+  bool ok = true;
+  for (int j = 0; j < k; ++j) {
+    const int e = ids[static_cast<size_t>(t) * k + j];
+    if (e < 0 || e >= E) ok = false;
+    for (int i = 0; i < j; ++i)
+      if (ids[static_cast<size_t>(t) * k + i] == e) ok = false;
+  }
+  if (!ok) {
+    set_status(status, MOE_ERR_DEVICE_CHECK);
+    return false;
+  }
+  for (int j = 0; j < k; ++j) {
+    const int e = ids[static_cast<size_t>(t) * k + j];
+    atomicOr(&mask[e * kMaskWords + (tl >> 5)], 1u << (tl & 31));
+  }
+  return true;
+}
+
+__device__ __forceinline__ int mask_count(const uint32_t* mask, int e) {
+  int c = 0;
+#pragma unroll
+  for (int w = 0; w < kMaskWords; ++w) c += __popc(mask[e * kMaskWords + w]);
+  return c;
+}
+
+__device__ __forceinline__ int mask_rank(const uint32_t* mask, int e, int tl) {
+  int c = 0;
+  const int wt = tl >> 5;
+  for (int w = 0; w < wt; ++w) c += __popc(mask[e * kMaskWords + w]);
+  return c + __popc(mask[e * kMaskWords + wt] & ((1u << (tl & 31)) - 1u));
+}
+
+// In-place exclusive scan of v[0..n) (n <= 4 * kTB) by a block of kTB
+// threads; returns the total.  Every thread must call it.
+__device__ int block_exclusive_scan(int* v, int n) {
+  __shared__ int warp_tot[kTB / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n + kTB - 1) / kTB;
+  const int i0 = tid * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i)
+    if (i0 + i < n) local += v[i0 + i];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int wbase = 0, total = 0;
+  for (int w = 0; w < kTB / 32; ++w) {
+    if (w < warp) wbase += warp_tot[w];
+    total += warp_tot[w];
+  }
+  int run = wbase + incl - local;
+  for (int i = 0; i < per; ++i)
+    if (i0 + i < n) {
+      const int c = v[i0 + i];
+      v[i0 + i] = run;
+      run += c;
+    }
+  __syncthreads();
+  return total;
+}
+
+// T <= kTB: the whole sort in one block.
+__global__ void __launch_bounds__(kTB)
+    permute_small_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_perm, int* status) {
+  __shared__ uint32_t mask[kMaxExperts * kMaskWords];
+  __shared__ int s_off[kMaxExperts];
+  const int t = threadIdx.x;
+  for (int i = t; i < E * kMaskWords; i += kTB) mask[i] = 0;
+  __syncthreads();
+  const bool valid = t < T && mask_token(ids, t, t, E, k, mask, status);
+  __syncthreads();
+  for (int e = t; e < E; e += kTB) s_off[e] = mask_count(mask, e);
+  __syncthreads();
+  const int total = block_exclusive_scan(s_off, E);
+  for (int e = t; e < E; e += kTB) offsets[e] = s_off[e];
+  if (t == 0) offsets[E] = total;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      if (valid) {
+        const int e = ids[static_cast<size_t>(t) * k + j];
+        const int r = s_off[e] + mask_rank(mask, e, t);
+        sorted_token[r] = t;
+        inv_perm[static_cast<size_t>(t) * k + j] = r;
+      } else {
+        inv_perm[static_cast<size_t>(t) * k + j] = -1;
+      }
+    }
+  }
+}
+
+// Large T, pass 1: per-block expert counts -> block_counts[b][E].
+__global__ void __launch_bounds__(kTB)
+    permute_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ block_counts,
+                         int* status) {
+  __shared__ uint32_t mask[kMaxExperts * kMaskWords];
+  const int tl = threadIdx.x, t = blockIdx.x * kTB + tl;
+  for (int i = tl; i < E * kMaskWords; i += kTB) mask[i] = 0;
+  __syncthreads();
+  if (t < T) mask_token(ids, t, tl, E, k, mask, status);
+  __syncthreads();
+  for (int e = tl; e < E; e += kTB) block_counts[static_cast<size_t>(blockIdx.x) * E + e] = mask_count(mask, e);
+}
+
+// Large T, pass 2 (one block): block_counts[b][e] -> first row of block b's
+// pairs of expert e; offsets[e] = exclusive scan of the expert totals.
+__global__ void __launch_bounds__(kTB)
+    permute_scan_kernel(int32_t* __restrict__ block_counts, int B, int E, int32_t* __restrict__ offsets) {
+  __shared__ int s_tot[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += kTB) {
+    int run = 0;
+    for (int b = 0; b < B; ++b) {
+      const int c = block_counts[static_cast<size_t>(b) * E + e];
+      block_counts[static_cast<size_t>(b) * E + e] = run;
+      run += c;
+    }
+    s_tot[e] = run;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(s_tot, E);
+  for (int e = threadIdx.x; e < E; e += kTB) {
+    offsets[e] = s_tot[e];
+    for (int b = 0; b < B; ++b) block_counts[static_cast<size_t>(b) * E + e] += s_tot[e];
+  }
+  if (threadIdx.x == 0) offsets[E] = total;
+}
+
+// Large T, pass 3: rows of every pair of the block.
+__global__ void __launch_bounds__(kTB)
+    permute_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
+                           const int32_t* __restrict__ block_base, int32_t* __restrict__ sorted_token,
+                           int32_t* __restrict__ inv_perm) {
+  __shared__ uint32_t mask[kMaxExperts * kMaskWords];
+  const int tl = threadIdx.x, t = blockIdx.x * kTB + tl;
+  for (int i = tl; i < E * kMaskWords; i += kTB) mask[i] = 0;
+  __syncthreads();
+  // errors were recorded by the count pass
+  const bool valid = t < T && mask_token(ids, t, tl, E, k, mask, nullptr);
+  __syncthreads();
+  if (t >= T) return;
+  const int32_t* base = block_base + static_cast<size_t>(blockIdx.x) * E;
+  for (int j = 0; j < k; ++j) {
+    if (valid) {
+      const int e = ids[static_cast<size_t>(t) * k + j];
+      const int r = base[e] + mask_rank(mask, e, tl);
+      sorted_token[r] = t;
+      inv_perm[static_cast<size_t>(t) * k + j] = r;
+    } else {
+      inv_perm[static_cast<size_t>(t) * k + j] = -1;
+    }
+  }
+}
+
+// x_perm[r] = x[sorted_token[r]] for r < offsets[E]; one warp per row, 16-byte
+// loads and stores.
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_token,
+                       const int32_t* __restrict__ offsets, int E, int T, int H, uint4* __restrict__ x_perm) {
+  const int rows = offsets[E];
+  const int vec = H / 8;
+  const int lane = threadIdx.x & 31;
+  for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += gridDim.x * 8) {
+    const int t = sorted_token[r];
+    if (t < 0 || t >= T) continue;
+    const uint4* src = x + static_cast<size_t>(t) * vec;
+    uint4* dst = x_perm + static_cast<size_t>(r) * vec;
+    for (int i = lane; i < vec; i += 32) dst[i] = src[i];
+  }
+}
+
+}  // namespace
+
+size_t permute_ws_bytes(int T, int E) {
+  const size_t B = (static_cast<size_t>(T) + kTB - 1) / kTB;
+  return T <= kTB ? 0 : align_up(B * E * sizeof(int32_t));
+}
+
+int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, int k, int32_t* offsets,
+                   int32_t* sorted_token, int32_t* inv_perm, void* x_perm, int32_t* block_counts, int* status,
+                   int num_sms, cudaStream_t stream, int* launches) {
+  if (T == 0) return MOE_OK;
+  if (T <= kTB) {
+    permute_small_kernel<<<1, kTB, 0, stream>>>(topk_ids, T, E, k, offsets, sorted_token, inv_perm, status);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    ++*launches;
+  } else {
+    const int B = (T + kTB - 1) / kTB;
+    permute_count_kernel<<<B, kTB, 0, stream>>>(topk_ids, T, E, k, block_counts, status);
+    permute_scan_kernel<<<1, kTB, 0, stream>>>(block_counts, B, E, offsets);
+    permute_scatter_kernel<<<B, kTB, 0, stream>>>(topk_ids, T, E, k, block_counts, sorted_token, inv_perm);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    *launches += 3;
+  }
+  if (x_perm) {
+    const long long rows = static_cast<long long>(T) * k;
+    long long grid = (rows + 7) / 8;
+    if (grid > 8LL * num_sms) grid = 8LL * num_sms;
+    gather_rows_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
+        static_cast<const uint4*>(x), sorted_token, offsets, E, T, H, static_cast<uint4*>(x_perm));
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    ++*launches;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,0 +1,309 @@
+"""Parity of each C-ABI call of the CUDA path with the CPU oracle, on seeded
+inputs, at sizes that span several tiles with ragged tails and at the full
+sizes of every workload (sampled rows where the oracle would take too long).
+
+Bars: expert ids, offsets and permutation indices bit-exact; the layer's bf16
+output within a relative Frobenius error of 1e-2 and a max abs error of
+2e-2 * max|ref| of the float64 oracle."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from cases import (ROUTE_W_ATOL, assert_close_layer, inputs, layer, routing, to_f64, x_tensor)
+from moe_ffn_layer_gb300 import binding as B
+from moe_ffn_layer_gb300 import build as build_mod
+from moe_ffn_layer_gb300 import synth
+from moe_ffn_layer_gb300.layer import MoEFFN, bf16_tensor
+from oracle import moe_oracle as om
+
+pytestmark = pytest.mark.gpu
+
+SMALL_SHAPES = [s for s in synth.FULL_SHAPES if s[1] <= 256]
+LARGE_SHAPES = [s for s in synth.FULL_SHAPES if s[1] > 256]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build_mod.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    L = B.lib()
+    yield L
+    torch.cuda.synchronize()
+
+
+def stream():
+    return torch.cuda.current_stream()
+
+
+def no_device_error():
+    assert B.moe_last_device_error(stream()) == 0
+
+
+def i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def f32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+# ---------------------------------------------------------------- a1 route
+
+@pytest.mark.parametrize("name,T", synth.FULL_SHAPES)
+def test_route(name, T):
+    w = synth.workload(name, T)
+    inp = inputs(name, T)
+    ids_ref, w_ref, *_ = routing(name, T)
+    x = bf16_tensor(inp["x"], "cuda")
+    wr = f32(inp["w_router"])
+    b = None if inp["bias"] is None else f32(inp["bias"])
+    ids = torch.empty((T, w.k), dtype=torch.int32, device="cuda")
+    tw = torch.empty((T, w.k), dtype=torch.float32, device="cuda")
+    nb = B.moe_route_workspace_bytes(T, w.E)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    B.moe_route(x, wr, b, T, w.H, w.E, w.k, ids, tw, ws, nb, stream())
+    no_device_error()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=0, atol=ROUTE_W_ATOL)
+
+
+# ---------------------------------------------------------------- a2 permute
+
+def _permute(ids_np, x_np, E, H, with_x=True):
+    T, k = ids_np.shape
+    ids = i32(ids_np)
+    x = bf16_tensor(x_np, "cuda") if with_x else None
+    off = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    st = torch.full((T * k,), -7, dtype=torch.int32, device="cuda")
+    inv = torch.full((T * k,), -7, dtype=torch.int32, device="cuda")
+    xp = torch.empty((T * k, H), dtype=torch.bfloat16, device="cuda") if with_x else None
+    nb = B.moe_permute_workspace_bytes(T, E)
+    ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+    B.moe_permute(ids, x, T, H, E, k, off, st, inv, xp, ws, nb, stream())
+    return off, st, inv, xp
+
+
+@pytest.mark.parametrize("name,T", synth.FULL_SHAPES)
+def test_permute(name, T):
+    w = synth.workload(name, T)
+    inp = inputs(name, T)
+    ids, _, off_ref, st_ref, inv_ref = routing(name, T)
+    off, st, inv, xp = _permute(ids, inp["x"], w.E, w.H)
+    no_device_error()
+    np.testing.assert_array_equal(off.cpu().numpy(), off_ref)
+    np.testing.assert_array_equal(st.cpu().numpy(), st_ref)
+    np.testing.assert_array_equal(inv.cpu().numpy(), inv_ref)
+    xp_bits = xp.view(torch.int16).cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(xp_bits, inp["x"][st_ref])
+
+
+@pytest.mark.parametrize("T", [255, 256, 257, 1000])
+def test_permute_block_boundaries(T):
+    """Both sort paths (one block for T <= 256, three passes above) around the
+    block size, with skewed ids, against the oracle."""
+    E, k = 37, 5
+    rng = np.random.default_rng(T)
+    p = 1.0 / np.arange(1, E + 1) ** 1.2
+    p /= p.sum()
+    # skewed, in no particular slot order
+    ids = np.stack([rng.permutation(rng.choice(E, size=k, replace=False, p=p)) for _ in range(T)]).astype(np.int32)
+    off_ref, st_ref, inv_ref = om.permute(ids, E)
+    off, st, inv, _ = _permute(ids, None, E, 64, with_x=False)
+    no_device_error()
+    np.testing.assert_array_equal(off.cpu().numpy(), off_ref)
+    np.testing.assert_array_equal(st.cpu().numpy(), st_ref)
+    np.testing.assert_array_equal(inv.cpu().numpy(), inv_ref)
+
+
+def test_permute_rejects_bad_ids():
+    """An id out of range or repeated within a token is recorded as a device
+    check error; that token's pairs get row -1 and nothing is written out of
+    bounds."""
+    ids = np.array([[0, 1], [2, 9], [3, 3], [1, 2]], dtype=np.int32)
+    off, st, inv, _ = _permute(ids, None, 4, 64, with_x=False)
+    assert B.moe_last_device_error(stream()) == -6
+    inv = inv.cpu().numpy().reshape(4, 2)
+    assert (inv[1] == -1).all() and (inv[2] == -1).all()
+    off = off.cpu().numpy()
+    assert off[-1] == 4          # only tokens 0 and 3 were sorted
+    assert B.moe_last_device_error(stream()) == 0   # read clears it
+
+
+# ---------------------------------------------------------------- a3/a4 grouped GEMM
+
+GEMM_CASES = [
+    # (group rows, N, K, act): weights-on-M form (few rows per group) ...
+    ([1, 0, 3, 16, 17, 64, 0, 2], 256, 128, 0),
+    ([1, 0, 3, 16, 17, 64, 0, 2], 128, 192, 1),
+    ([100, 0, 5, 200, 1, 63, 65, 0], 384, 256, 1),     # groups over one 64-row chunk
+    ([100, 0, 5, 200, 1, 63, 65, 0], 256, 128, 0),
+    # ... and tokens-on-M form (many rows per group): ragged 128-row tiles
+    ([127, 129, 0, 300], 256, 192, 1),
+    ([127, 129, 0, 300], 192, 128, 0),
+    ([127, 129, 0, 300], 384, 64, 0),
+    ([128, 1, 255, 0, 257], 128, 256, 1),
+    ([64, 1000], 192, 64, 1),
+    ([513], 512, 128, 0),
+]
+
+
+@pytest.mark.parametrize("rows,N,K,act", GEMM_CASES)
+def test_grouped_gemm(rows, N, K, act):
+    G = len(rows)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    R = int(off[-1])
+    rows_max = R + 5           # rows past the last group must stay untouched
+    a_bits = synth.random_bf16((rows_max, K), seed=R + N, tag=51)
+    w_bits = synth.random_bf16((G, 2 * N if act else N, K), seed=K + G, tag=52, sigma=0.05)
+    ref = om.grouped_gemm(a_bits, w_bits, off, act)
+    a = bf16_tensor(a_bits, "cuda")
+    w = bf16_tensor(w_bits, "cuda")
+    out = torch.full((rows_max, N), 1024.0, dtype=torch.bfloat16, device="cuda")
+    B.moe_grouped_gemm(a, w, i32(off), G, rows_max, N, K, act, out, stream())
+    no_device_error()
+    got = to_f64(out)
+    assert_close_layer(got[:R], ref[:R], f"gemm rows={rows} N={N} K={K} act={act}")
+    assert np.all(got[R:] == 1024.0)
+    # per-row check as well: no row may be far off even if the total is fine
+    for r in np.linspace(0, R - 1, min(R, 16)).astype(int):
+        scale = np.abs(ref[r]).max() + 1e-6
+        assert np.abs(got[r] - ref[r]).max() <= 2e-2 * scale, r
+
+
+@pytest.mark.parametrize("T,N,K,act", [(1, 256, 128, 1), (37, 128, 256, 0), (200, 256, 128, 1), (300, 128, 64, 0)])
+def test_grouped_gemm_single_group_no_offsets(T, N, K, act):
+    """G = 1 without an offsets array: the shared expert's form."""
+    a_bits = synth.random_bf16((T, K), seed=T, tag=53)
+    w_bits = synth.random_bf16((1, 2 * N if act else N, K), seed=N, tag=54, sigma=0.05)
+    ref = om.grouped_gemm(a_bits, w_bits, np.array([0, T]), act)
+    out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    B.moe_grouped_gemm(bf16_tensor(a_bits, "cuda"), bf16_tensor(w_bits, "cuda"), None, 1, T, N, K, act, out,
+                       stream())
+    no_device_error()
+    assert_close_layer(to_f64(out), ref, "single group")
+
+
+def test_grouped_gemm_rejects_bad_offsets():
+    """Offsets past rows_max or decreasing: the kernel records a device check
+    error and computes nothing."""
+    a = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((2, 128, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((64, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    for bad in ([0, 10, 80], [0, 30, 20]):
+        offs = i32(bad)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        B.moe_grouped_gemm(a, w, offs, 2, 64, 128, 64, 0, out, stream())
+        torch.cuda.synchronize()
+        # the kernel leaves at once: no bounded wait ran out
+        assert time.perf_counter() - t0 < 0.5
+        assert B.moe_last_device_error(stream()) == -6
+    assert torch.all(out == 7.0)
+
+
+# ---------------------------------------------------------------- a6 combine
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("decode", 8), ("batched_decode", 256)])
+def test_combine(name, T):
+    w = synth.workload(name, T)
+    _, wts, _, _, inv = routing(name, T)
+    y_bits = synth.random_bf16((T * w.k, w.H), seed=T, tag=55)
+    s_bits = synth.random_bf16((T, w.H), seed=T, tag=56)
+    ref = om.combine(om.bf16_to_f64(y_bits), inv, wts, om.bf16_to_f64(s_bits))
+    out = torch.empty((T, w.H), dtype=torch.bfloat16, device="cuda")
+    B.moe_unpermute_combine(bf16_tensor(y_bits, "cuda"), i32(inv), f32(wts), bf16_tensor(s_bits, "cuda"), T, w.H,
+                            w.k, out, stream())
+    no_device_error()
+    got = to_f64(out)
+    # fp32 accumulation, one rounding to bf16: within one bf16 ulp of the exact sum
+    np.testing.assert_allclose(got, ref, rtol=2.0 ** -8, atol=1e-5)
+    # without the shared row
+    B.moe_unpermute_combine(bf16_tensor(y_bits, "cuda"), i32(inv), f32(wts), None, T, w.H, w.k, out, stream())
+    ref0 = om.combine(om.bf16_to_f64(y_bits), inv, wts, None)
+    np.testing.assert_allclose(to_f64(out), ref0, rtol=2.0 ** -8, atol=1e-5)
+
+
+# ---------------------------------------------------------------- whole layer
+
+@pytest.mark.parametrize("name,T", SMALL_SHAPES)
+def test_forward_full(name, T):
+    w = synth.workload(name, T)
+    inp = inputs(name, T)
+    ref = om.forward(inp, w.k)
+    L = layer(name, T)
+    out = L.forward(x_tensor(name, T))
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], f"{name} T={T}")
+
+
+def _sample_tokens(name, T, n=24):
+    ids, _, off, st, _ = routing(name, T)
+    rng = np.random.default_rng(7)
+    pick = set(rng.choice(T, size=n, replace=False).tolist()) | {0, T - 1}
+    counts = np.diff(off)
+    hot = int(np.argmax(counts))
+    # tokens at the ends of the hottest group and of a 128-row tile boundary inside it
+    g0, g1 = int(off[hot]), int(off[hot + 1])
+    for r in (g0, g1 - 1, min(g0 + 127, g1 - 1), min(g0 + 128, g1 - 1)):
+        pick.add(int(st[r]))
+    return np.array(sorted(pick))
+
+
+@pytest.mark.parametrize("name,T", LARGE_SHAPES)
+def test_forward_sampled_full_size(name, T):
+    """Full-size prefill layers: every output is finite, and sampled rows
+    (random tokens plus tokens at the hot group's tile boundaries) match the
+    oracle evaluated token by token."""
+    w = synth.workload(name, T)
+    inp = inputs(name, T)
+    ids, wts, *_ = routing(name, T)
+    L = layer(name, T)
+    out = L.forward(x_tensor(name, T))
+    no_device_error()
+    toks = _sample_tokens(name, T)
+    ref = om.forward_tokens(inp, w.k, toks, routing=(ids, wts))
+    got = out[torch.from_numpy(toks).cuda()]
+    assert torch.isfinite(out.float()).all()
+    assert_close_layer(to_f64(got), ref["out"], f"{name} T={T} sampled")
+
+
+def test_forward_one_hot_expert_and_empty_experts():
+    """Every token routed to one expert (a group of T rows spanning several
+    128-row tiles with a ragged tail) while most experts stay empty; T above
+    the one-block permute size."""
+    wl = synth.Workload("hot", 300, 256, 16, 2, 128, 128, sigma_router=0.1)
+    inp = synth.make_inputs(wl, 11)
+    bias = np.zeros(wl.E, dtype=np.float32)
+    bias[5] = 50.0
+    bias[[0, 1, 2, 3]] = -np.inf
+    inp["bias"] = bias
+    ref = om.forward(inp, wl.k)
+    assert (np.diff(ref["offsets"])[5] == wl.T)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    out = L.forward(bf16_tensor(inp["x"], "cuda"))
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], "hot expert")
+
+
+def test_forward_without_shared_expert():
+    wl = synth.Workload("noshared", 40, 128, 8, 2, 64, 0, sigma_router=0.1)
+    inp = synth.make_inputs(wl, 12)
+    ref = om.forward(inp, wl.k)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    out = L.forward(bf16_tensor(inp["x"], "cuda"))
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], "no shared expert")
+
+
+def test_forward_repeatable_and_launch_count():
+    """Two calls give identical bits; the launch count is what the call reports."""
+    L = layer("tiny", 16)
+    x = x_tensor("tiny", 16)
+    a = L.forward(x).clone()
+    n = B.moe_last_launch_count()
+    b = L.forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert n >= 6
