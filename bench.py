@@ -191,6 +191,8 @@ def run_gpu(args, w):
     wgt_bytes = (2 * w.I * w.H + w.H * w.I) * 2
     touched = min(w.E, w.T * w.k) * wgt_bytes + 6 * w.H * w.Is
     R = int(min(16, max(2, -(-4 * L2_BYTES // max(touched, 1)))))
+    if args.copies:
+        R = args.copies
     layers = [base]
     for _ in range(R - 1):
         t = base.tensors
@@ -266,12 +268,15 @@ def run_gpu(args, w):
         # dominant kernel: the routed gate_up GroupedMatmul, timed alone on the
         # layer's own dispatched rows, back to back in one graph over the weight copies
         h = torch.empty((w.T * w.k, w.I), dtype=torch.bfloat16, device=dev)
+        gb_ws = B.moe_grouped_gemm_workspace_bytes(w.E, w.T * w.k, w.I, w.H, 1)
+        g_ws = torch.zeros(max(gb_ws, 256), dtype=torch.uint8, device=dev)
         M = max(20, min(400, K))
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             cs = torch.cuda.current_stream()
             for i in range(M):
-                B.moe_grouped_gemm(xperm, layers[i % R].tensors[2], offs, w.E, w.T * w.k, w.I, w.H, 1, h, cs)
+                B.moe_grouped_gemm(xperm, layers[i % R].tensors[2], offs, w.E, w.T * w.k, w.I, w.H, 1, h, g_ws,
+                                   gb_ws, cs)
         with torch.cuda.stream(stream):
             g.replay()
             e0.record(stream)
@@ -410,6 +415,7 @@ def main():
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate over (0: enough to defeat L2)")
     args = ap.parse_args()
     from moe_ffn_layer_gb300 import synth
     T = args.T if args.T is not None else (8 if args.workload == "decode" else None)

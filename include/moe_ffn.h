@@ -123,10 +123,18 @@ MOE_API int moe_permute(const int32_t* topk_ids, const void* x, int T, int H, in
  *                means one group covering rows [0, rows_max) (requires G == 1)
  *  rows_max      host upper bound on group_offsets[G] (device-checked)
  *  out           bf16 [rows_max][N]; rows outside every group are not written
+ *  ws            split-K scratch of moe_grouped_gemm_workspace_bytes(...) bytes,
+ *                256-byte aligned, or NULL (no split-K).  It must be zero-filled
+ *                before its first use; every call leaves its counters zero
+ *                again (after a device error, zero it again).  Calls that share
+ *                a scratch buffer must not overlap on the GPU.
  * bf16 inputs, fp32 accumulation in tensor memory, bf16 (round-to-nearest)
- * output.  Supported: K % 64 == 0, N % 64 == 0, G <= 1024. */
+ * output.  Split-K (only for groups of at most 16 rows, weights-on-M form)
+ * adds fp32 partials in a fixed order: results do not depend on scheduling.
+ * Supported: K % 64 == 0, N % 64 == 0, G <= 1024. */
+MOE_API size_t moe_grouped_gemm_workspace_bytes(int G, int rows_max, int N, int K, int act);
 MOE_API int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max, int N,
-                     int K, int act, void* out, cudaStream_t stream);
+                             int K, int act, void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Combine: out[t] = bf16( sum_j topk_w[t,j] * y[inv_perm[t*k+j]] + shared[t] ),
  * accumulated in fp32 in slot order j = 0..k-1, then the shared row.
@@ -141,7 +149,10 @@ MOE_API int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const 
  * `stream`, waited by `side`) and ev_join (recorded on `side`, waited by
  * `stream` before the combine).  Exactly one fork and one join event per call.
  * `side` and the events may be NULL when d->I_s == 0.  ws holds every
- * intermediate; size it with moe_workspace_bytes(d, T).
+ * intermediate and the split-K scratch of the four matmuls; size it with
+ * moe_workspace_bytes(d, T), align it to 256 bytes and zero-fill it before its
+ * first use (calls leave the scratch counters zero).  Calls that share a
+ * workspace must not overlap on the GPU.
  *  x bf16 [T][H] (device);  out bf16 [T][H] (device) */
 MOE_API size_t moe_workspace_bytes(const moe_dims* d, int T);
 MOE_API int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, void* out, void* ws,

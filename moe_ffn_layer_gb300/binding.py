@@ -40,7 +40,8 @@ _SIGS = {
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_permute_workspace_bytes": (_Z, [_I, _I]),
     "moe_permute": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
-    "moe_grouped_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_grouped_gemm_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
+    "moe_grouped_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_unpermute_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_workspace_bytes": (_Z, [ctypes.POINTER(moe_dims), _I]),
     "moe_forward": (_I, [ctypes.POINTER(moe_dims), ctypes.POINTER(moe_weights), _P, _I, _P, _P, _Z, _P, _P, _P,
@@ -120,9 +121,13 @@ def moe_permute(topk_ids, x, T, H, E, k, expert_offsets, sorted_token, inv_perm,
                                                    ws_bytes, handle(stream)))
 
 
-def moe_grouped_gemm(a, w, group_offsets, G, rows_max, N, K, act, out, stream) -> int:
+def moe_grouped_gemm_workspace_bytes(G, rows_max, N, K, act) -> int:
+    return lib().moe_grouped_gemm_workspace_bytes(G, rows_max, N, K, act)
+
+
+def moe_grouped_gemm(a, w, group_offsets, G, rows_max, N, K, act, out, ws, ws_bytes, stream) -> int:
     return _check("moe_grouped_gemm", lib().moe_grouped_gemm(ptr(a), ptr(w), ptr(group_offsets), G, rows_max, N, K,
-                                                             act, ptr(out), handle(stream)))
+                                                             act, ptr(out), ptr(ws), ws_bytes, handle(stream)))
 
 
 def moe_unpermute_combine(y, inv_perm, topk_w, shared, T, H, k, out, stream) -> int:

@@ -9,6 +9,7 @@
 // drops the per-step dispatch/combine/gmm2 events once the overlap exists and
 // preallocates events instead of creating them per step: here the caller owns
 // exactly two events and the library creates none.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -50,6 +51,7 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) 
 
 // Every intermediate of moe_forward, 256-byte aligned, in one caller-owned buffer.
 struct Layout {
+  size_t gemm_main, gemm_main_bytes, gemm_side, gemm_side_bytes;
   size_t logits, ids, w, offsets, sorted, inv, pcounts, xperm, h, y, hs, s, total;
 };
 
@@ -62,6 +64,16 @@ Layout layout(const moe_dims* d, int T) {
     return r;
   };
   const size_t Tk = static_cast<size_t>(T) * d->k;
+  // split-K scratch: one region for the routed pair (main stream), one for the
+  // shared pair (side stream), so the two streams never share counters
+  const int rows = T * d->k;
+  L.gemm_main_bytes = std::max(moe::grouped_gemm_ws_bytes(d->E, rows, d->I, 1),
+                               moe::grouped_gemm_ws_bytes(d->E, rows, d->H, 0));
+  L.gemm_side_bytes = d->I_s ? std::max(moe::grouped_gemm_ws_bytes(1, T, d->I_s, 1),
+                                        moe::grouped_gemm_ws_bytes(1, T, d->H, 0))
+                             : 0;
+  L.gemm_main = take(L.gemm_main_bytes);
+  L.gemm_side = take(L.gemm_side_bytes);
   L.logits = take(moe::route_ws_bytes(T, d->E));
   L.ids = take(Tk * 4);
   L.w = take(Tk * 4);
@@ -109,8 +121,8 @@ int moe_route(const void* x, const float* w_router, const float* bias, int T, in
     return MOE_ERR_UNSUPPORTED;
   if (ws_bytes < moe::route_ws_bytes(T, E)) return MOE_ERR_WORKSPACE;
   int n = 0;
-  const int rc = moe::route_launch(x, w_router, bias, T, H, E, k, topk_ids, topk_w, static_cast<float*>(ws), stream,
-                                   &n);
+  const int rc = moe::route_launch(x, w_router, bias, T, H, E, k, topk_ids, topk_w, static_cast<float*>(ws),
+                                   nullptr, stream, &n);
   t_last_launches = n;
   return rc;
 }
@@ -143,21 +155,29 @@ int moe_permute(const int32_t* topk_ids, const void* x, int T, int H, int E, int
   return rc;
 }
 
+size_t moe_grouped_gemm_workspace_bytes(int G, int rows_max, int N, int K, int act) {
+  if (G <= 0 || rows_max < 0 || N <= 0 || K <= 0 || (act != 0 && act != 1)) return 0;
+  return moe::grouped_gemm_ws_bytes(G, rows_max, N, act);
+}
+
 int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max, int N, int K,
-                     int act, void* out, cudaStream_t stream) {
+                     int act, void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
   t_last_launches = 0;
   if (G <= 0 || rows_max < 0 || N <= 0 || K <= 0 || (act != 0 && act != 1)) return MOE_ERR_INVALID;
   if (!group_offsets && G != 1) return MOE_ERR_INVALID;
   if (G > moe::grouped_gemm_max_groups() || N % 64 || K % 64) return MOE_ERR_UNSUPPORTED;
   if (rows_max == 0) return MOE_OK;
   if (!a || !w || !out) return MOE_ERR_INVALID;
-  if (!al16(a) || !al16(w) || !al16(out) || (reinterpret_cast<uintptr_t>(group_offsets) & 3u))
+  if (!al16(a) || !al16(w) || !al16(out) || (reinterpret_cast<uintptr_t>(group_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
     return MOE_ERR_UNSUPPORTED;
   DevInfo* di = nullptr;
   int rc = dev_info(&di);
   if (rc) return rc;
+  if (ws && ws_bytes < moe::grouped_gemm_ws_bytes(G, rows_max, N, act)) return MOE_ERR_WORKSPACE;
   int n = 0;
-  rc = moe::grouped_gemm_launch(a, w, group_offsets, G, rows_max, N, K, act, out, di->status, di->sms, stream, &n);
+  rc = moe::grouped_gemm_launch(a, w, group_offsets, G, rows_max, N, K, act, out, di->status, ws, ws_bytes, di->sms,
+                                stream, &n);
   t_last_launches = n;
   return rc;
 }
@@ -216,6 +236,8 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
   void* y = base + L.y;
   void* hs = base + L.hs;
   void* s = base + L.s;
+  void* gmain = base + L.gemm_main;
+  void* gside = base + L.gemm_side;
   const int rows = T * d->k;
   int n = 0;
 
@@ -223,25 +245,32 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
   if (has_shared) {
     if (cudaEventRecord(ev_fork, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamWaitEvent(side, ev_fork, 0) != cudaSuccess) return MOE_ERR_CUDA;
-    rc = moe::grouped_gemm_launch(x, w->ws_gate_up, nullptr, 1, T, d->I_s, d->H, 1, hs, di->status, di->sms, side,
-                                  &n);
+    rc = moe::grouped_gemm_launch(x, w->ws_gate_up, nullptr, 1, T, d->I_s, d->H, 1, hs, di->status, gside,
+                                  L.gemm_side_bytes, di->sms, side, &n);
     if (!rc)
-      rc = moe::grouped_gemm_launch(hs, w->ws_down, nullptr, 1, T, d->H, d->I_s, 0, s, di->status, di->sms, side,
-                                    &n);
+      rc = moe::grouped_gemm_launch(hs, w->ws_down, nullptr, 1, T, d->H, d->I_s, 0, s, di->status, gside,
+                                    L.gemm_side_bytes, di->sms, side, &n);
     if (rc) return rc;
     if (cudaEventRecord(ev_join, side) != cudaSuccess) return MOE_ERR_CUDA;
   }
   // routed path on `stream`: route -> dispatch -> gmm1 (+SiLU*mul) -> gmm2
-  rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, stream, &n);
+  if (T <= moe::route_small_max_tokens()) {
+    // decode sizes: router, top-k, counting sort and row gather in one launch
+    const moe::DispatchOut dout{offsets, sorted, inv, xperm};
+    rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, &dout, stream, &n);
+  } else {
+    rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, nullptr, stream,
+                           &n);
+    if (!rc)
+      rc = moe::permute_launch(ids, x, T, d->H, d->E, d->k, offsets, sorted, inv, xperm, pcounts, di->status,
+                               di->sms, stream, &n);
+  }
   if (!rc)
-    rc = moe::permute_launch(ids, x, T, d->H, d->E, d->k, offsets, sorted, inv, xperm, pcounts, di->status, di->sms,
-                             stream, &n);
+    rc = moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, gmain,
+                                  L.gemm_main_bytes, di->sms, stream, &n);
   if (!rc)
-    rc = moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, di->sms,
-                                  stream, &n);
-  if (!rc)
-    rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, di->sms, stream,
-                                  &n);
+    rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, gmain,
+                                  L.gemm_main_bytes, di->sms, stream, &n);
   if (rc) return rc;
   // join, then combine
   if (has_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;

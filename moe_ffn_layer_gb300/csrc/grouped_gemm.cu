@@ -15,7 +15,10 @@
 //  WEIGHTS_ON_M (decode; few rows per group, weight streaming): a unit is 128
 //    weight rows x up to NMAX token rows.  A = weight tile [128 x 64 K] (for
 //    SiLU*mul: a gate tile and the matching up tile, two MMAs), B = token tile
-//    loaded in 16-row boxes, MMA N = token rows rounded up to 16.
+//    loaded in 16-row boxes, MMA N = token rows rounded up to 16.  The K steps
+//    go round-robin to up to 4 accumulator chains: an MMA this small is cheap,
+//    but one that adds into the accumulator of the MMA just before it waits
+//    for it, which would cap the weight stream of an SM far below HBM speed.
 //
 // Roles:  warp 0      TMA producer into a STAGES-deep shared-memory ring
 //         warp 1      tensor-memory allocator and MMA issuer (one thread)
@@ -25,6 +28,15 @@
 // weight blocks; empty groups contribute none.  Units are ordered (group,
 // weight block, row block) so that CTAs running side by side share a weight
 // block in L2.
+//
+// Split-K (weights-on-M form, every group <= 16 rows, scratch given): when the
+// units do not spread evenly over the grid, every CTA picks the same split S
+// in {1, 2, 4, 8} from the unit count; sub-unit (u, s) covers K blocks
+// [s*KB/S, (s+1)*KB/S).  Each sub-unit stores its fp32 partial accumulator,
+// then takes a ticket on the unit's counter; the ticket holder that arrives
+// last adds the S partials in split order (its own from registers), resets the
+// counter to zero and runs the epilogue.  The result does not depend on which
+// CTA arrives last, and no CTA waits for another.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -57,6 +69,9 @@ struct Cfg {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
+constexpr int kSplitRows = 16;     // split-K only when every group has <= 16 rows
+constexpr int kMaxSplit = 8;
+
 struct GemmArgs {
   const int32_t* offsets;  // [G+1] or nullptr (one group [0, rows_max))
   int G;
@@ -66,7 +81,25 @@ struct GemmArgs {
   __nv_bfloat16* out;      // [rows_max][N]
   int* status;
   int stream_w;            // weights streamed once: evict-first in L2
+  int* counters;           // split-K tickets, one per unit, zero between calls (nullptr: no split)
+  float* partials;         // split-K partial accumulators, split_cap slots
+  int split_cap;           // sub-units the scratch holds
+  int unit_cap;            // units the counters cover
 };
+
+// fp32 values one TMEM lane keeps per split-K partial
+template <int ACT>
+constexpr int partial_floats() { return (ACT ? 2 : 1) * kSplitRows; }
+
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Weights-on-M form: K steps are spread over C independent accumulator chains
+// (chain = K step mod C) so that consecutive small-N MMAs do not wait on one
+// another; the epilogue adds the chains in order.  C is the largest of 4, 2, 1
+// whose chains fit the unit's tensor-memory columns.
+__host__ __device__ constexpr int swap_chains(int n16, int acc_cols, int act) {
+  return 4 * (act ? 2 : 1) * n16 * 16 <= acc_cols ? 4 : (2 * (act ? 2 : 1) * n16 * 16 <= acc_cols ? 2 : 1);
+}
 
 template <int SWAP, int W, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -85,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
+  int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] split S, [1] last arriver, [2..5] warp ok
   int* s_off = reinterpret_cast<int*>(smem + C::kStages * C::kStageBytes + 256);   // [G+1]
   int* s_ustart = s_off + (kMaxGroups + 1);                                          // [G+1]
 
@@ -93,22 +127,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = args.G;
   const int NB = args.N / C::kOutCols;   // weight blocks per group
 
-  // ---- group table: offsets and unit prefix (warp 0), barriers (warp 1)
+  // ---- group offsets into shared memory (all threads), barriers (warp 1)
+  for (int i = threadIdx.x; i <= G; i += kThreads)
+    s_off[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows_max);
+  if (warp == 1 && lane == 0) {
+    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int kblocks = args.K / kBK;
+  // ---- unit table (warp 0): checks, unit prefix per group, split choice
   if (warp == 0) {
     const int per = (G + 31) / 32;
     const int g0 = lane * per;
-    int local = 0;
+    int local = 0, mx = 0;
     bool bad = false;
     for (int i = 0; i < per; ++i) {
       const int g = g0 + i;
       if (g < G) {
-        int a, b;
-        if (args.offsets) { a = args.offsets[g]; b = args.offsets[g + 1]; }
-        else { a = 0; b = args.rows_max; }
+        const int a = s_off[g], b = s_off[g + 1];
         if (a < 0 || b < a || b > args.rows_max) bad = true;
-        s_off[g] = a;
-        if (g == G - 1) s_off[G] = b;
-        local += ((b - a + C::kUnitRows - 1) / C::kUnitRows) * NB;
+        const int rows = bad ? 0 : b - a;
+        mx = max(mx, rows);
+        s_ustart[g] = local;
+        local += ((rows + C::kUnitRows - 1) / C::kUnitRows) * NB;
       }
     }
     int incl = local;
@@ -117,34 +161,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    int run = incl - local;
-    for (int i = 0; i < per; ++i) {
-      const int g = g0 + i;
-      if (g < G) {
-        s_ustart[g] = run;
-        int a, b;
-        if (args.offsets) { a = args.offsets[g]; b = args.offsets[g + 1]; }
-        else { a = 0; b = args.rows_max; }
-        run += ((b - a + C::kUnitRows - 1) / C::kUnitRows) * NB;
-      }
-    }
+    const int base = incl - local;
+    for (int i = 0; i < per; ++i)
+      if (g0 + i < G) s_ustart[g0 + i] += base;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     const bool any_bad = __any_sync(0xffffffffu, bad);
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int units = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) {
-      *s_total = any_bad ? 0 : total;
+      int S = 1;
+      if (SWAP && args.counters && mx <= kSplitRows && units <= args.unit_cap) {
+        // sub-units per CTA x (K blocks per sub-unit + a fixed cost of 2 blocks)
+        const int grid = static_cast<int>(gridDim.x);
+        long long best = static_cast<long long>((units + grid - 1) / grid) * (kblocks + 2);
+        for (int c = 2; c <= kMaxSplit; c *= 2) {
+          if (kblocks % c || static_cast<long long>(units) * c > args.split_cap) continue;
+          const long long cost = ((static_cast<long long>(units) * c + grid - 1) / grid) * (kblocks / c + 2);
+          if (cost < best) { best = cost; S = c; }
+        }
+      }
+      s_split[0] = S;
+      *s_total = any_bad ? 0 : units * S;
       *abort_flag = 0;
       if (any_bad && blockIdx.x == 0) set_status(args.status, MOE_ERR_DEVICE_CHECK);
       tma_prefetch_desc(&tm_tok);
       tma_prefetch_desc(&tm_wgt);
     }
-  } else if (warp == 1 && lane == 0) {
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
-    mbar_init(done_bar, 1);
-    fence_barrier_init();
   }
   __syncthreads();
   const int total = *s_total;
+  const int S = s_split[0];
+  const int kb_per = kblocks / S;
   // a CTA without units (or every CTA, when the offsets failed their check)
   // leaves before it allocates tensor memory
   if (static_cast<int>(blockIdx.x) >= total) return;
@@ -174,7 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     nrows = min(rows - rb * C::kUnitRows, C::kUnitRows);
   };
 
-  const int kblocks = args.K / kBK;
   const int wrows = ACT ? 2 * args.N : args.N;   // weight rows per group
 
   if (warp == 0) {
@@ -186,14 +232,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
+        const int u = idx / S, sp = idx - u * S;
         int g, row0, nrows, wb;
-        decode(idx, g, row0, nrows, wb);
+        decode(u, g, row0, nrows, wb);
         const int wrow = g * wrows + wb * C::kOutCols;
         const int n16 = (nrows + 15) >> 4;
         const uint32_t bytes = SWAP ? static_cast<uint32_t>(C::kABytes + n16 * 16 * kBK * 2)
                                     : static_cast<uint32_t>(C::kStageBytes);
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = sp * kb_per; kb < (sp + 1) * kb_per; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status)) { ok = false; break; }
           uint8_t* sa = stage_base + stage * C::kStageBytes;
           uint8_t* sb = sa + C::kABytes;
@@ -234,19 +281,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int idx = blockIdx.x; idx < total; idx += gridDim.x, ++it) {
         const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
         const uint32_t aphase = (C::kNumAcc == 2 ? (it >> 1) : it) & 1;
+        const int u = idx / S, sp = idx - u * S;
         uint32_t idesc;
+        int chains = 1, cw = 0;
         if (SWAP) {
           int g, row0, nrows, wb;
-          decode(idx, g, row0, nrows, wb);
-          idesc = idesc_bf16_f32(128, ((nrows + 15) >> 4) * 16);
+          decode(u, g, row0, nrows, wb);
+          const int n16 = (nrows + 15) >> 4;
+          idesc = idesc_bf16_f32(128, n16 * 16);
+          chains = swap_chains(n16, C::kAccCols, ACT);
+          cw = n16 * 16;
         } else {
           idesc = idesc_bf16_f32(128, W);
         }
         if (!mbar_wait(&tempty_bar[ab], aphase ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * C::kAccCols;
+        const int kb0 = sp * kb_per;
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb0 + kb_per; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * C::kStageBytes);
@@ -256,12 +309,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // +32 bytes per 16-element K step inside the 128-byte swizzle row
-            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-            umma_bf16(d_tmem, da + static_cast<uint64_t>(kk * 2), db + static_cast<uint64_t>(kk * 2), idesc, acc);
-            if (SWAP && ACT) {
-              const uint64_t du = smem_desc_k128(sa + kTileRows128);
-              umma_bf16(d_tmem + W, du + static_cast<uint64_t>(kk * 2), db + static_cast<uint64_t>(kk * 2), idesc,
-                        acc);
+            const uint64_t ka = static_cast<uint64_t>(kk * 2);
+            if (SWAP) {
+              const int c = kk & (chains - 1);
+              const uint32_t acc = (kb > kb0 || kk >= chains) ? 1u : 0u;
+              umma_bf16(d_tmem + c * cw, da + ka, db + ka, idesc, acc);
+              if (ACT) {
+                const uint64_t du = smem_desc_k128(sa + kTileRows128);
+                umma_bf16(d_tmem + (chains + c) * cw, du + ka, db + ka, idesc, acc);
+              }
+            } else {
+              umma_bf16(d_tmem, da + ka, db + ka, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
             }
           }
           umma_commit(&empty_bar[stage]);      // frees the smem stage when these MMAs finish
@@ -282,33 +340,123 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = blockIdx.x; idx < total; idx += gridDim.x, ++it) {
       const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
       const uint32_t aphase = (C::kNumAcc == 2 ? (it >> 1) : it) & 1;
+      const int u = idx / S, sp = idx - u * S;
       int g, row0, nrows, wb;
-      decode(idx, g, row0, nrows, wb);
-      if (!mbar_wait(&tfull_bar[ab], aphase, abort_flag, args.status)) break;
+      decode(u, g, row0, nrows, wb);
+      bool ok = mbar_wait(&tfull_bar[ab], aphase, abort_flag, args.status);
+      if (S > 1) {
+        // the split path meets at named barriers: the four warps leave together or not at all
+        if (lane == 0) s_split[2 + q] = ok ? 1 : 0;
+        epi_bar_sync();
+        ok = s_split[2] && s_split[3] && s_split[4] && s_split[5];
+      }
+      if (!ok) break;
       tc_fence_after();
       const uint32_t t_acc = tmem_base + ab * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[ab]);
+      };
       if (SWAP) {
-        // accumulator row = output column wb*128 + lrow; accumulator column = token
+        // accumulator row = output column wb*128 + lrow; accumulator column =
+        // token, chain c of gate (h = 0) / up (h = 1) at column (h*C + c)*cw
         __nv_bfloat16* ocol = args.out + static_cast<size_t>(row0) * args.N + wb * 128 + lrow;
-#pragma unroll 1
-        for (int c = 0; c < nrows; c += 32) {
-          uint32_t gr[32];
-          tmem_ld_32cols(t_acc + c, gr);
-          if (ACT) {
-            uint32_t ur[32];
-            tmem_ld_32cols(t_acc + W + c, ur);
+        const int n16 = (nrows + 15) >> 4;
+        const int chains = swap_chains(n16, C::kAccCols, ACT);
+        const int cw = n16 * 16;
+        // sums of the chains for tokens [16j, 16j + 16): gs (gate or plain), us (up)
+        auto load_chunk = [&](int j, float (&gs)[16], float (&us)[16]) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) { gs[i] = 0.f; us[i] = 0.f; }
+          for (int c = 0; c < chains; ++c) {
+            uint32_t r[16];
+            tmem_ld_16cols(t_acc + c * cw + j * 16, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float gv = __uint_as_float(gr[i]);
-              gr[i] = __float_as_uint(gv / (1.0f + __expf(-gv)) * __uint_as_float(ur[i]));
-            }
-          } else {
-            tmem_ld_wait();
+            for (int i = 0; i < 16; ++i) gs[i] += __uint_as_float(r[i]);
           }
+          if (ACT) {
+            for (int c = 0; c < chains; ++c) {
+              uint32_t r[16];
+              tmem_ld_16cols(t_acc + (chains + c) * cw + j * 16, r);
+              tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c + i < nrows) ocol[static_cast<size_t>(c + i) * args.N] = __float2bfloat16_rn(__uint_as_float(gr[i]));
+              for (int i = 0; i < 16; ++i) us[i] += __uint_as_float(r[i]);
+            }
+          }
+        };
+        if (S == 1) {
+#pragma unroll 1
+          for (int j = 0; j < n16; ++j) {
+            float gs[16], us[16];
+            load_chunk(j, gs, us);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              if (j * 16 + i < nrows) {
+                const float h = ACT ? gs[i] / (1.0f + __expf(-gs[i])) * us[i] : gs[i];
+                ocol[static_cast<size_t>(j * 16 + i) * args.N] = __float2bfloat16_rn(h);
+              }
+            }
+          }
+          release_acc();
+        } else {
+          // split-K: nrows <= 16, one 16-token chunk holds the whole partial
+          constexpr int PF = partial_floats<ACT>();
+          float gm[16], um[16];
+          load_chunk(0, gm, um);
+          release_acc();
+          float4* mine = reinterpret_cast<float4*>(args.partials + (static_cast<size_t>(idx) * 128 + lrow) * PF);
+#pragma unroll
+          for (int i = 0; i < kSplitRows / 4; ++i) {
+            mine[i] = make_float4(gm[4 * i], gm[4 * i + 1], gm[4 * i + 2], gm[4 * i + 3]);
+            if (ACT) mine[kSplitRows / 4 + i] = make_float4(um[4 * i], um[4 * i + 1], um[4 * i + 2], um[4 * i + 3]);
+          }
+          __threadfence();
+          epi_bar_sync();
+          if (threadIdx.x == 64) {
+            const int old = atomicAdd(&args.counters[u], 1);
+            int last = 0;
+            if (old == S - 1) {
+              last = 1;
+              atomicExch(&args.counters[u], 0);   // every ticket of this unit is taken: back to zero
+            } else if (old < 0 || old >= S) {
+              set_status(args.status, MOE_ERR_DEVICE_CHECK);   // counters were not zero at entry
+            }
+            s_split[1] = last;
+          }
+          epi_bar_sync();
+          if (s_split[1]) {
+            __threadfence();
+            float gs[kSplitRows], us[kSplitRows];
+#pragma unroll
+            for (int i = 0; i < kSplitRows; ++i) { gs[i] = 0.f; us[i] = 0.f; }
+            for (int j = 0; j < S; ++j) {   // split order, whoever arrived last
+              if (j == sp) {
+#pragma unroll
+                for (int i = 0; i < kSplitRows; ++i) { gs[i] += gm[i]; us[i] += um[i]; }
+              } else {
+                const float4* src = reinterpret_cast<const float4*>(
+                    args.partials + (static_cast<size_t>(u * S + j) * 128 + lrow) * PF);
+#pragma unroll
+                for (int i = 0; i < kSplitRows / 4; ++i) {
+                  const float4 v = __ldcg(src + i);
+                  gs[4 * i] += v.x; gs[4 * i + 1] += v.y; gs[4 * i + 2] += v.z; gs[4 * i + 3] += v.w;
+                  if (ACT) {
+                    const float4 w4 = __ldcg(src + kSplitRows / 4 + i);
+                    us[4 * i] += w4.x; us[4 * i + 1] += w4.y; us[4 * i + 2] += w4.z; us[4 * i + 3] += w4.w;
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < kSplitRows; ++i) {
+              if (i < nrows) {
+                const float h = ACT ? gs[i] / (1.0f + __expf(-gs[i])) * us[i] : gs[i];
+                ocol[static_cast<size_t>(i) * args.N] = __float2bfloat16_rn(h);
+              }
+            }
+          }
         }
       } else {
         // accumulator row = token row0 + lrow; accumulator column = output column
@@ -350,10 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        release_acc();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[ab]);
     }
   }
 
@@ -398,9 +544,35 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Split-K scratch of one weights-on-M launch: a ticket counter per unit and
+// fp32 partial slots (at most kMaxSlots sub-units).
+struct SplitPlan {
+  int unit_cap = 0;
+  int split_cap = 0;
+  size_t counter_bytes = 0;
+  size_t bytes = 0;
+};
+
+constexpr int kSwapRows = 64;   // token rows per unit in the weights-on-M form
+constexpr int kMaxSlots = 4096;
+
+SplitPlan split_plan(int G, int rows_max, int N, int act) {
+  SplitPlan p;
+  if (rows_max <= 0 || N % 128 || static_cast<long long>(rows_max) > 64LL * G) return p;
+  const long long nonempty = G < rows_max ? G : rows_max;
+  const long long units = ((rows_max + kSwapRows - 1) / kSwapRows + nonempty) * (N / 128);
+  const long long cap = units * kMaxSplit < kMaxSlots ? units * kMaxSplit : kMaxSlots;
+  p.unit_cap = static_cast<int>(units);
+  p.split_cap = static_cast<int>(cap);
+  p.counter_bytes = align_up(static_cast<size_t>(units) * sizeof(int));
+  const size_t slot = 128 * static_cast<size_t>(act ? partial_floats<1>() : partial_floats<0>()) * sizeof(float);
+  p.bytes = p.counter_bytes + static_cast<size_t>(cap) * slot;
+  return p;
+}
+
 template <int SWAP, int W, int ACT>
 int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K, void* out,
-               int* status, int grid_cap, cudaStream_t stream, int* launches) {
+               int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream, int* launches) {
   using C = Cfg<SWAP, W, ACT>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -419,12 +591,22 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   if (!make_map(&tw, w, static_cast<uint64_t>(G) * wrows, static_cast<uint64_t>(K), wgt_box)) return MOE_ERR_CUDA;
   // upper bound on the unit count: every non-empty group adds at most one partial row block
   const long long nonempty = offsets ? (G < rows_max ? G : rows_max) : 1;
-  const long long bound =
+  long long bound =
       (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) * (N / C::kOutCols);
+  GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
+                nullptr, nullptr, 0, 0};
+  if (SWAP && ws) {
+    const SplitPlan p = split_plan(G, rows_max, N, ACT);
+    if (p.bytes && ws_bytes >= p.bytes) {
+      args.counters = static_cast<int*>(ws);
+      args.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + p.counter_bytes);
+      args.unit_cap = p.unit_cap;
+      args.split_cap = p.split_cap;
+      bound *= kMaxSplit;
+    }
+  }
   int grid = static_cast<int>(bound < grid_cap ? bound : grid_cap);
   if (grid < 1) grid = 1;
-  const int stream_w = SWAP ? 1 : 0;
-  GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, stream_w};
   grouped_gemm_kernel<SWAP, W, ACT><<<grid, kThreads, C::kSmemBytes, stream>>>(tt, tw, args);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
@@ -437,20 +619,35 @@ bool grouped_gemm_weights_on_m(int G, int rows_max, int N) {
   return N % 128 == 0 && static_cast<long long>(rows_max) <= 64LL * G;
 }
 
+size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act) {
+  return split_plan(G, rows_max, N, act).bytes;
+}
+
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
-                        int act, void* out, int* status, int grid_cap, cudaStream_t stream, int* launches) {
+                        int act, void* out, int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream,
+                        int* launches) {
   if (rows_max == 0) return MOE_OK;
   if (grouped_gemm_weights_on_m(G, rows_max, N)) {
-    if (act == 1) return launch_cfg<1, 64, 1>(a, w, offsets, G, rows_max, N, K, out, status, grid_cap, stream, launches);
-    return launch_cfg<1, 64, 0>(a, w, offsets, G, rows_max, N, K, out, status, grid_cap, stream, launches);
+    if (act == 1)
+      return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap,
+                                         stream, launches);
+    return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap, stream,
+                                       launches);
   }
   if (act == 1) {
-    if (N % 128 == 0) return launch_cfg<0, 256, 1>(a, w, offsets, G, rows_max, N, K, out, status, grid_cap, stream, launches);
-    return launch_cfg<0, 128, 1>(a, w, offsets, G, rows_max, N, K, out, status, grid_cap, stream, launches);
+    if (N % 128 == 0)
+      return launch_cfg<0, 256, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
+                                   launches);
+    return launch_cfg<0, 128, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
+                                 launches);
   }
-  if (N % 256 == 0) return launch_cfg<0, 256, 0>(a, w, offsets, G, rows_max, N, K, out, status, grid_cap, stream, launches);
-  if (N % 128 == 0) return launch_cfg<0, 128, 0>(a, w, offsets, G, rows_max, N, K, out, status, grid_cap, stream, launches);
-  return launch_cfg<0, 64, 0>(a, w, offsets, G, rows_max, N, K, out, status, grid_cap, stream, launches);
+  if (N % 256 == 0)
+    return launch_cfg<0, 256, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
+                                 launches);
+  if (N % 128 == 0)
+    return launch_cfg<0, 128, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
+                                 launches);
+  return launch_cfg<0, 64, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream, launches);
 }
 
 int grouped_gemm_max_groups() { return kMaxGroups; }

@@ -9,9 +9,20 @@
 
 namespace moe {
 
+// Dispatch outputs the small-T router can produce in the same launch.
+struct DispatchOut {
+  int32_t* offsets;
+  int32_t* sorted_token;
+  int32_t* inv_perm;
+  void* x_perm;   // may be nullptr
+};
+
 size_t route_ws_bytes(int T, int E);
+int route_small_max_tokens();
+// dispatch != nullptr requires T <= route_small_max_tokens().
 int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
-                 int32_t* topk_ids, float* topk_w, float* logits_ws, cudaStream_t stream, int* launches);
+                 int32_t* topk_ids, float* topk_w, float* logits_ws, const DispatchOut* dispatch, cudaStream_t stream,
+                 int* launches);
 
 size_t permute_ws_bytes(int T, int E);
 int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, int k, int32_t* offsets,
@@ -19,8 +30,12 @@ int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, 
                    int num_sms, cudaStream_t stream, int* launches);
 
 bool grouped_gemm_weights_on_m(int G, int rows_max, int N);
+// Split-K scratch bytes of a launch (0: never splits).
+size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act);
+// ws (nullable): split-K scratch, zero-filled before its first use; left zero.
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
-                        int act, void* out, int* status, int grid_cap, cudaStream_t stream, int* launches);
+                        int act, void* out, int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream,
+                        int* launches);
 int grouped_gemm_max_groups();
 
 int combine_launch(const void* y, const int32_t* inv_perm, const float* topk_w, const void* shared, int T, int H,

@@ -9,74 +9,30 @@
 // precision (fp32), the top-k and the renormalisation are the layer's
 // definition in its benchmark shapes.
 //
-// Logit kernels:
-//   T <= 16   router_gemv: one warp per (expert, quarter of H), every token at
-//             once; streams Wr (E*H*4 bytes) once.  Decode shapes.
-//   T >  16   router_tile: fp32 SIMT tile GEMM, 64 tokens x 64 experts per CTA.
-// Then topk_softmax: one warp per token.
+// Kernels:
+//   T <= 16   route_small: one 8-CTA thread-block cluster does the whole
+//             router (and, inside the layer forward, the dispatch too): each
+//             warp streams one (expert, H slice) of Wr once and dots it with
+//             every token; partial logits go to CTA 0's shared memory through
+//             distributed shared memory; after a cluster barrier CTA 0 adds
+//             them in slice order, takes the top-k, and (optionally) runs the
+//             counting sort; after a second barrier all CTAs gather the rows.
+//             Decode shapes: one launch instead of four, no global counters.
+//   T >  16   router_tile (fp32 SIMT tile GEMM, 64 tokens x 64 experts per
+//             CTA) then topk_softmax (one warp per token).
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 namespace {
 
-constexpr int kGemvMaxT = 16;
-constexpr int kGemvSlices = 4;   // warps sharing one expert's dot products
-constexpr int kGemvExpertsPerCta = 2;
-
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
   f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
-// grid: ceil(E / kGemvExpertsPerCta) CTAs of kGemvExpertsPerCta * kGemvSlices warps.
-// Warp (e, s) sums h in {s*256 + lane*8 + i*kGemvSlices*256 .. +8}; the slices are
-// added in slice order, so the result does not depend on scheduling.
-__global__ void __launch_bounds__(kGemvExpertsPerCta* kGemvSlices * 32)
-    router_gemv_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr,
-                       const float* __restrict__ bias, int T, int H, int E, float* __restrict__ logits) {
-  __shared__ float part[kGemvExpertsPerCta][kGemvSlices][kGemvMaxT];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int le = warp / kGemvSlices, s = warp % kGemvSlices;
-  const int e = blockIdx.x * kGemvExpertsPerCta + le;
-  float acc[kGemvMaxT];
-#pragma unroll
-  for (int t = 0; t < kGemvMaxT; ++t) acc[t] = 0.f;
-  if (e < E) {
-    const float* w = wr + static_cast<size_t>(e) * H;
-#pragma unroll 2
-    for (int h0 = s * 256 + lane * 8; h0 < H; h0 += kGemvSlices * 256) {
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + h0));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + h0 + 4));
-#pragma unroll
-      for (int t = 0; t < kGemvMaxT; ++t) {
-        if (t < T) {
-          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + h0));
-          float f[8];
-          bf16x8_to_f32(xv, f);
-          float a = acc[t];
-          a = fmaf(f[0], w0.x, a); a = fmaf(f[1], w0.y, a); a = fmaf(f[2], w0.z, a); a = fmaf(f[3], w0.w, a);
-          a = fmaf(f[4], w1.x, a); a = fmaf(f[5], w1.y, a); a = fmaf(f[6], w1.z, a); a = fmaf(f[7], w1.w, a);
-          acc[t] = a;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kGemvMaxT; ++t) {
-    float v = acc[t];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) part[le][s][t] = v;
-  }
-  __syncthreads();
-  if (e < E && s == 0 && lane < T) {
-    float v = 0.f;
-#pragma unroll
-    for (int q = 0; q < kGemvSlices; ++q) v += part[le][q][lane];
-    if (bias) v += bias[e];
-    logits[static_cast<size_t>(lane) * E + e] = v;
-  }
 }
 
 // fp32 SIMT GEMM: logits[T][E] = x[T][H] . Wr[E][H]^T (+ b).  CTA tile 64 x 64,
@@ -136,28 +92,24 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// One warp per token: k rounds of a warp arg-max over the E logits (larger
-// value wins, equal values go to the lower id), then the chosen ids are sorted
-// ascending and w_j = exp(l_j - max) / sum_i exp(l_i - max) over the chosen k.
+// Top-k of one token by one warp: k rounds of a warp arg-max over the E
+// logits (larger value wins, equal values go to the lower id); round r's
+// winner stays in lane r.  The chosen ids are then ranked by id across lanes
+// (ascending order), and w_j = exp(l_j - max) / sum_i exp(l_i - max) over the
+// chosen k, the sum taken by a fixed butterfly.  Registers only.
 constexpr int kTopkMaxPerLane = kMaxExperts / 32;
 
-__global__ void __launch_bounds__(256)
-    topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
-                        float* __restrict__ topk_w) {
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+__device__ void warp_topk_softmax(const float* l, int E, int k, int32_t* ids_out, float* w_out) {
   const int lane = threadIdx.x & 31;
-  if (t >= T) return;
   float v[kTopkMaxPerLane];
-  const float* l = logits + static_cast<size_t>(t) * E;
 #pragma unroll
   for (int i = 0; i < kTopkMaxPerLane; ++i) {
     const int e = i * 32 + lane;
     v[i] = e < E ? l[e] : -INFINITY;
   }
   uint32_t taken = 0;   // bit i: element i of this lane already chosen
-  int ids[kMaxTopK];
-  float vals[kMaxTopK];
-#pragma unroll 1
+  int my_id = 0x7fffffff;
+  float my_v = -INFINITY;
   for (int r = 0; r < k; ++r) {
     float best = -INFINITY;
     int bid = 0x7fffffff;
@@ -172,48 +124,193 @@ __global__ void __launch_bounds__(256)
       const int oi = __shfl_xor_sync(0xffffffffu, bid, o);
       if (ob > best || (ob == best && oi < bid)) { best = ob; bid = oi; }
     }
-    ids[r] = bid;
-    vals[r] = best;
+    if (lane == r) { my_id = bid; my_v = best; }
     if (bid < E && (bid & 31) == lane) taken |= 1u << (bid >> 5);
   }
-  if (lane != 0) return;
-  // insertion sort of the chosen (id, logit) pairs by id
-  for (int i = 1; i < k; ++i) {
-    const int ci = ids[i];
-    const float cv = vals[i];
-    int j = i - 1;
-    while (j >= 0 && ids[j] > ci) { ids[j + 1] = ids[j]; vals[j + 1] = vals[j]; --j; }
-    ids[j + 1] = ci;
-    vals[j + 1] = cv;
+  // position of this lane's id among the chosen ids
+  int rank = 0;
+  for (int j = 0; j < k; ++j) rank += __shfl_sync(0xffffffffu, my_id, j) < my_id ? 1 : 0;
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);   // round 0 took the maximum
+  const float p = lane < k ? expf(my_v - m) : 0.f;
+  float sum = p;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    ids_out[rank] = my_id;
+    w_out[rank] = p / sum;
   }
-  float m = -INFINITY;
-  for (int i = 0; i < k; ++i) m = fmaxf(m, vals[i]);
-  float p[kMaxTopK];
-  float s = 0.f;
-  for (int i = 0; i < k; ++i) { p[i] = expf(vals[i] - m); s += p[i]; }
-  const float inv = 1.0f / s;
-  for (int i = 0; i < k; ++i) {
-    topk_ids[static_cast<size_t>(t) * k + i] = ids[i];
-    topk_w[static_cast<size_t>(t) * k + i] = p[i] * inv;
+}
+
+__global__ void __launch_bounds__(256)
+    topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
+                        float* __restrict__ topk_w) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  warp_topk_softmax(logits + static_cast<size_t>(t) * E, E, k, topk_ids + static_cast<size_t>(t) * k,
+                    topk_w + static_cast<size_t>(t) * k);
+}
+
+// ---------------------------------------------------------------- T <= 16: one cluster
+
+constexpr int kSmallT = 16;
+constexpr int kClusterCtas = 8;
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kClusterCtas * kSmallThreads / 32;   // 256 warps in the cluster
+
+struct SmallArgs {
+  const __nv_bfloat16* x;
+  const float* wr;
+  const float* bias;
+  int T, H, E, k, S;          // S: H slices per expert
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* offsets;           // nullptr: route only
+  int32_t* sorted_token;
+  int32_t* inv_perm;
+  __nv_bfloat16* x_perm;      // nullptr: no row gather
+};
+
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kSmallThreads, 1)
+    route_small_kernel(const SmallArgs a) {
+  __shared__ float part[kSmallT * kMaxExperts];   // [S][T][E]; S * E <= max(256, E)
+  __shared__ int32_t s_ids[kSmallT * kMaxTopK];
+  __shared__ float s_w[kSmallT * kMaxTopK];
+  __shared__ uint32_t s_mask[kMaxExperts];
+  __shared__ int s_off[kMaxExperts];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, H = a.H, E = a.E, k = a.k, S = a.S;
+  const int HS = H / S;
+  float* part0 = cluster.map_shared_rank(part, 0);
+
+  // ---- partial logits: warp task (e, s) dots Wr[e, s-th slice] with every token
+  for (int task = rank * (kSmallThreads / 32) + warp; task < E * S; task += kSmallWarps) {
+    const int e = task / S, sl = task % S;
+    float acc[kSmallT];
+#pragma unroll
+    for (int t = 0; t < kSmallT; ++t) acc[t] = 0.f;
+    const float* w = a.wr + static_cast<size_t>(e) * H;
+#pragma unroll 2
+    for (int h0 = sl * HS + lane * 8; h0 < (sl + 1) * HS; h0 += 256) {
+      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + h0));
+      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + h0 + 4));
+#pragma unroll
+      for (int t = 0; t < kSmallT; ++t) {
+        if (t < T) {
+          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * H + h0));
+          float f[8];
+          bf16x8_to_f32(xv, f);
+          float v = acc[t];
+          v = fmaf(f[0], w0.x, v); v = fmaf(f[1], w0.y, v); v = fmaf(f[2], w0.z, v); v = fmaf(f[3], w0.w, v);
+          v = fmaf(f[4], w1.x, v); v = fmaf(f[5], w1.y, v); v = fmaf(f[6], w1.z, v); v = fmaf(f[7], w1.w, v);
+          acc[t] = v;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kSmallT; ++t) {
+      if (t < T) {
+        float v = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) part0[(sl * T + t) * E + e] = v;
+      }
+    }
   }
+  cluster.sync();
+
+  if (rank == 0) {
+    // ---- logits = slices added in order (+ bias), in place in slice 0
+    for (int i = threadIdx.x; i < T * E; i += kSmallThreads) {
+      float v = part[i];
+      for (int sl = 1; sl < S; ++sl) v += part[sl * T * E + i];
+      if (a.bias) v += a.bias[i % E];
+      part[i] = v;
+    }
+    __syncthreads();
+    if (warp < T) warp_topk_softmax(part + warp * E, E, k, s_ids + warp * k, s_w + warp * k);
+    __syncthreads();
+    for (int i = threadIdx.x; i < T * k; i += kSmallThreads) {
+      a.topk_ids[i] = s_ids[i];
+      a.topk_w[i] = s_w[i];
+    }
+    if (a.offsets) {
+      // ---- counting sort by (expert, token): token bitmask per expert
+      for (int e = threadIdx.x; e < E; e += kSmallThreads) s_mask[e] = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < T * k; i += kSmallThreads) atomicOr(&s_mask[s_ids[i]], 1u << (i / k));
+      __syncthreads();
+      if (warp == 0) {   // exclusive scan of the counts over experts
+        int run = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+          const int e = e0 + lane;
+          const int c = e < E ? __popc(s_mask[e]) : 0;
+          int incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+          }
+          if (e < E) s_off[e] = run + incl - c;
+          run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) a.offsets[E] = run;
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < E; e += kSmallThreads) a.offsets[e] = s_off[e];
+      for (int i = threadIdx.x; i < T * k; i += kSmallThreads) {
+        const int t = i / k, e = s_ids[i];
+        const int r = s_off[e] + __popc(s_mask[e] & ((1u << t) - 1u));
+        a.sorted_token[r] = t;
+        a.inv_perm[i] = r;
+      }
+    }
+  }
+  if (a.x_perm) {
+    // the barrier's release/acquire makes CTA 0's sorted_token stores visible
+    cluster.sync();
+    // ---- row gather: x_perm[r] = x[sorted[r]], one warp per row across the cluster
+    const int vec = H / 8;
+    for (int r = rank * (kSmallThreads / 32) + warp; r < T * k; r += kSmallWarps) {
+      const int t = a.sorted_token[r];
+      const uint4* src = reinterpret_cast<const uint4*>(a.x) + static_cast<size_t>(t) * vec;
+      uint4* dst = reinterpret_cast<uint4*>(a.x_perm) + static_cast<size_t>(r) * vec;
+      for (int i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
+    }
+  }
+  // other CTAs touch CTA 0's shared memory only before the first barrier
 }
 
 }  // namespace
 
 size_t route_ws_bytes(int T, int E) { return align_up(static_cast<size_t>(T) * E * sizeof(float)); }
 
+int route_small_max_tokens() { return kSmallT; }
+
 int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
-                 int32_t* topk_ids, float* topk_w, float* logits_ws, cudaStream_t stream, int* launches) {
+                 int32_t* topk_ids, float* topk_w, float* logits_ws, const DispatchOut* dispatch, cudaStream_t stream,
+                 int* launches) {
   if (T == 0) return MOE_OK;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  if (T <= kGemvMaxT) {
-    const int grid = (E + kGemvExpertsPerCta - 1) / kGemvExpertsPerCta;
-    router_gemv_kernel<<<grid, kGemvExpertsPerCta * kGemvSlices * 32, 0, stream>>>(xb, w_router, bias, T, H, E,
-                                                                                   logits_ws);
-  } else {
-    dim3 grid((T + kRT - 1) / kRT, (E + kRE - 1) / kRE);
-    router_tile_kernel<<<grid, 256, 0, stream>>>(xb, w_router, bias, T, H, E, logits_ws);
+  if (T <= kSmallT) {
+    int S = kSmallWarps / E;
+    if (S < 1) S = 1;
+    while (S > 1 && H % (S * 8)) --S;
+    SmallArgs a{xb, w_router, bias, T, H, E, k, S, topk_ids, topk_w, nullptr, nullptr, nullptr, nullptr};
+    if (dispatch) {
+      a.offsets = dispatch->offsets;
+      a.sorted_token = dispatch->sorted_token;
+      a.inv_perm = dispatch->inv_perm;
+      a.x_perm = static_cast<__nv_bfloat16*>(dispatch->x_perm);
+    }
+    route_small_kernel<<<kClusterCtas, kSmallThreads, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    ++*launches;
+    return MOE_OK;
   }
+  dim3 grid((T + kRT - 1) / kRT, (E + kRE - 1) / kRE);
+  router_tile_kernel<<<grid, 256, 0, stream>>>(xb, w_router, bias, T, H, E, logits_ws);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
   topk_softmax_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits_ws, T, E, k, topk_ids, topk_w);

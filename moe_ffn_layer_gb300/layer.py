@@ -52,9 +52,11 @@ class MoEFFN:
         return B.moe_workspace_bytes(self.dims, T)
 
     def workspace(self, T: int) -> torch.Tensor:
+        """Workspace for batches of up to T tokens, zero-filled when allocated
+        (the library keeps its scratch counters zero from call to call)."""
         need = self.workspace_bytes(T)
         if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+            self._ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
         return self._ws
 
     def forward(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

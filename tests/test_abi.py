@@ -55,6 +55,10 @@ def test_workspace_queries(lib):
     assert B.moe_route_workspace_bytes(16, 128) >= 16 * 128 * 4
     assert B.moe_permute_workspace_bytes(256, 128) == 0          # one-block path needs none
     assert B.moe_permute_workspace_bytes(4096, 128) >= 16 * 128 * 4
+    # split-K scratch only for the weights-on-M form (few rows per group)
+    assert B.moe_grouped_gemm_workspace_bytes(128, 64, 768, 2048, 1) > 0
+    assert B.moe_grouped_gemm_workspace_bytes(128, 65536, 768, 2048, 1) == 0
+    assert B.moe_grouped_gemm_workspace_bytes(128, 64, 768, 2048, 1) >= 128 * 64 * 4
 
 
 def _rc(fn, *args):
@@ -67,13 +71,15 @@ def test_host_side_argument_checks(lib):
     INVALID, UNSUP = -1, -2
     fake = 1 << 20    # never dereferenced: every call below returns before a launch
     # grouped GEMM: N, K multiples of 64; act 0/1; groups need offsets unless G == 1
-    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 8, 64, 100, 64, 0, fake, None) == UNSUP
-    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 8, 64, 128, 96, 0, fake, None) == UNSUP
-    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 8, 64, 128, 64, 2, fake, None) == INVALID
-    assert _rc(B.moe_grouped_gemm, fake, fake, None, 8, 64, 128, 64, 0, fake, None) == INVALID
-    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 2000, 64, 128, 64, 0, fake, None) == UNSUP
-    assert _rc(B.moe_grouped_gemm, fake + 8, fake, fake, 8, 64, 128, 64, 0, fake, None) == UNSUP
-    assert B.moe_grouped_gemm(fake, fake, fake, 8, 0, 128, 64, 0, fake, None) == 0    # no rows: no-op
+    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 8, 64, 100, 64, 0, fake, None, 0, None) == UNSUP
+    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 8, 64, 128, 96, 0, fake, None, 0, None) == UNSUP
+    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 8, 64, 128, 64, 2, fake, None, 0, None) == INVALID
+    assert _rc(B.moe_grouped_gemm, fake, fake, None, 8, 64, 128, 64, 0, fake, None, 0, None) == INVALID
+    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 2000, 64, 128, 64, 0, fake, None, 0, None) == UNSUP
+    assert _rc(B.moe_grouped_gemm, fake + 8, fake, fake, 8, 64, 128, 64, 0, fake, None, 0, None) == UNSUP
+    assert B.moe_grouped_gemm(fake, fake, fake, 8, 0, 128, 64, 0, fake, None, 0, None) == 0    # no rows: no-op
+    # split-K scratch must be 256-byte aligned
+    assert _rc(B.moe_grouped_gemm, fake, fake, fake, 8, 64, 128, 64, 0, fake, fake + 16, 1 << 20, None) == UNSUP
     # router: k <= E, E <= 512, k <= 16, H % 8
     assert _rc(B.moe_route, fake, fake, None, 4, 64, 8, 9, fake, fake, fake, 1 << 20, None) == INVALID
     assert _rc(B.moe_route, fake, fake, None, 4, 64, 1024, 8, fake, fake, fake, 1 << 20, None) == UNSUP

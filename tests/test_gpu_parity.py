@@ -69,6 +69,24 @@ def test_route(name, T):
     np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=0, atol=ROUTE_W_ATOL)
 
 
+@pytest.mark.parametrize("T,H,E,k", [(1, 256, 8, 2), (5, 520, 8, 3), (16, 2048, 64, 6), (16, 512, 512, 16),
+                                     (3, 4096, 256, 8), (17, 256, 40, 4)])
+def test_route_shapes(T, H, E, k):
+    """The one-cluster router (T <= 16) across slice counts, E up to 512 and
+    k up to 16, and the tiled router just above it."""
+    w = synth.Workload("r", T, H, E, k, 64, 0, sigma_router=0.3, zipf_s=1.0)
+    x_np, wr_np, b_np = synth.make_activations(w, 4)
+    ids_ref, w_ref, _ = om.route(x_np, wr_np, b_np, k)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    tw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    nb = B.moe_route_workspace_bytes(T, E)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    B.moe_route(bf16_tensor(x_np, "cuda"), f32(wr_np), f32(b_np), T, H, E, k, ids, tw, ws, nb, stream())
+    no_device_error()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=0, atol=ROUTE_W_ATOL)
+
+
 # ---------------------------------------------------------------- a2 permute
 
 def _permute(ids_np, x_np, E, H, with_x=True):
@@ -137,6 +155,10 @@ GEMM_CASES = [
     # (group rows, N, K, act): weights-on-M form (few rows per group) ...
     ([1, 0, 3, 16, 17, 64, 0, 2], 256, 128, 0),
     ([1, 0, 3, 16, 17, 64, 0, 2], 128, 192, 1),
+    ([1, 0, 3, 16, 2, 0, 9, 1], 256, 512, 1),           # every group <= 16 rows: split-K applies
+    ([1, 0, 3, 16, 2, 0, 9, 1], 384, 2048, 0),
+    ([1] * 8 + [0] * 100 + [2, 16], 128, 1024, 1),      # few units, many groups
+    ([5], 2048, 768, 0),
     ([100, 0, 5, 200, 1, 63, 65, 0], 384, 256, 1),     # groups over one 64-row chunk
     ([100, 0, 5, 200, 1, 63, 65, 0], 256, 128, 0),
     # ... and tokens-on-M form (many rows per group): ragged 128-row tiles
@@ -149,8 +171,9 @@ GEMM_CASES = [
 ]
 
 
+@pytest.mark.parametrize("use_ws", [False, True])
 @pytest.mark.parametrize("rows,N,K,act", GEMM_CASES)
-def test_grouped_gemm(rows, N, K, act):
+def test_grouped_gemm(rows, N, K, act, use_ws):
     G = len(rows)
     off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
     R = int(off[-1])
@@ -160,12 +183,20 @@ def test_grouped_gemm(rows, N, K, act):
     ref = om.grouped_gemm(a_bits, w_bits, off, act)
     a = bf16_tensor(a_bits, "cuda")
     w = bf16_tensor(w_bits, "cuda")
+    nb = B.moe_grouped_gemm_workspace_bytes(G, rows_max, N, K, act)
+    ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda") if use_ws else None
     out = torch.full((rows_max, N), 1024.0, dtype=torch.bfloat16, device="cuda")
-    B.moe_grouped_gemm(a, w, i32(off), G, rows_max, N, K, act, out, stream())
+    B.moe_grouped_gemm(a, w, i32(off), G, rows_max, N, K, act, out, ws, nb if use_ws else 0, stream())
     no_device_error()
     got = to_f64(out)
     assert_close_layer(got[:R], ref[:R], f"gemm rows={rows} N={N} K={K} act={act}")
     assert np.all(got[R:] == 1024.0)
+    if use_ws:   # the scratch counters are back to zero, and a second call gives the same bits
+        assert int(ws[:nb].view(torch.int32)[: 64].abs().sum()) == 0 or nb == 0
+        out2 = torch.full_like(out, 1024.0)
+        B.moe_grouped_gemm(a, w, i32(off), G, rows_max, N, K, act, out2, ws, nb, stream())
+        no_device_error()
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     # per-row check as well: no row may be far off even if the total is fine
     for r in np.linspace(0, R - 1, min(R, 16)).astype(int):
         scale = np.abs(ref[r]).max() + 1e-6
@@ -179,7 +210,9 @@ def test_grouped_gemm_single_group_no_offsets(T, N, K, act):
     w_bits = synth.random_bf16((1, 2 * N if act else N, K), seed=N, tag=54, sigma=0.05)
     ref = om.grouped_gemm(a_bits, w_bits, np.array([0, T]), act)
     out = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
-    B.moe_grouped_gemm(bf16_tensor(a_bits, "cuda"), bf16_tensor(w_bits, "cuda"), None, 1, T, N, K, act, out,
+    nb = B.moe_grouped_gemm_workspace_bytes(1, T, N, K, act)
+    ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+    B.moe_grouped_gemm(bf16_tensor(a_bits, "cuda"), bf16_tensor(w_bits, "cuda"), None, 1, T, N, K, act, out, ws, nb,
                        stream())
     no_device_error()
     assert_close_layer(to_f64(out), ref, "single group")
@@ -195,7 +228,7 @@ def test_grouped_gemm_rejects_bad_offsets():
         offs = i32(bad)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        B.moe_grouped_gemm(a, w, offs, 2, 64, 128, 64, 0, out, stream())
+        B.moe_grouped_gemm(a, w, offs, 2, 64, 128, 64, 0, out, None, 0, stream())
         torch.cuda.synchronize()
         # the kernel leaves at once: no bounded wait ran out
         assert time.perf_counter() - t0 < 0.5
