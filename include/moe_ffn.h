@@ -136,6 +136,27 @@ MOE_API size_t moe_grouped_gemm_workspace_bytes(int G, int rows_max, int N, int 
 MOE_API int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max, int N,
                              int K, int act, void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* moe_grouped_gemm for callers that cannot allocate device memory: for
+ * example code that runs inside another runtime's execution step, where a
+ * cudaMalloc is forbidden or would stall the stream, or that must leave every
+ * device allocation to an allocator it does not own.  Same arguments, result
+ * and checks as moe_grouped_gemm, without the ws/ws_bytes pair: the split-K
+ * scratch is a fixed array of MOE_NOALLOC_SCRATCH_BYTES in the library's own
+ * device memory, held on every GPU that loads the library until the process
+ * exits.  The pages describe no such call; it is an addition of this library.
+ *  - Allocates nothing: no cudaMalloc or cudaFree, no allocating library call.
+ *    It clears the scratch counters with cudaMemsetAsync on `stream`.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - Every call uses the same array and it keeps the previous call's data:
+ *    calls that overlap on the GPU (other streams, other threads) race on it
+ *    and give wrong results.  Order them on one stream.
+ *  - A problem whose scratch would exceed the array returns MOE_ERR_WORKSPACE. */
+#define MOE_NOALLOC_SCRATCH_BYTES (24u << 20)
+MOE_API int moe_grouped_gemm_noalloc(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max,
+                                     int N, int K, int act, void* out, cudaStream_t stream);
+
 /* Combine: out[t] = bf16( sum_j topk_w[t,j] * y[inv_perm[t*k+j]] + shared[t] ),
  * accumulated in fp32 in slot order j = 0..k-1, then the shared row.
  *  y bf16 [T*k][H];  inv_perm int32 [T*k];  topk_w fp32 [T][k]

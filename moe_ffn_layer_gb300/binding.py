@@ -42,6 +42,7 @@ _SIGS = {
     "moe_permute": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_grouped_gemm_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "moe_grouped_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_grouped_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "moe_unpermute_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_workspace_bytes": (_Z, [ctypes.POINTER(moe_dims), _I]),
     "moe_forward": (_I, [ctypes.POINTER(moe_dims), ctypes.POINTER(moe_weights), _P, _I, _P, _P, _Z, _P, _P, _P,
@@ -128,6 +129,12 @@ def moe_grouped_gemm_workspace_bytes(G, rows_max, N, K, act) -> int:
 def moe_grouped_gemm(a, w, group_offsets, G, rows_max, N, K, act, out, ws, ws_bytes, stream) -> int:
     return _check("moe_grouped_gemm", lib().moe_grouped_gemm(ptr(a), ptr(w), ptr(group_offsets), G, rows_max, N, K,
                                                              act, ptr(out), ptr(ws), ws_bytes, handle(stream)))
+
+
+def moe_grouped_gemm_noalloc(a, w, group_offsets, G, rows_max, N, K, act, out, stream) -> int:
+    return _check("moe_grouped_gemm_noalloc", lib().moe_grouped_gemm_noalloc(ptr(a), ptr(w), ptr(group_offsets), G,
+                                                                             rows_max, N, K, act, ptr(out),
+                                                                             handle(stream)))
 
 
 def moe_unpermute_combine(y, inv_perm, topk_w, shared, T, H, k, out, stream) -> int:

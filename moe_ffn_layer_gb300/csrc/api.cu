@@ -102,6 +102,17 @@ int check_dims(const moe_dims* d) {
 
 }  // namespace
 
+namespace moe {
+int current_device_info(int** status, int* num_sms) {
+  DevInfo* di = nullptr;
+  const int rc = dev_info(&di);
+  if (rc) return rc;
+  *status = di->status;
+  *num_sms = di->sms;
+  return MOE_OK;
+}
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_route_workspace_bytes(int T, int E) {

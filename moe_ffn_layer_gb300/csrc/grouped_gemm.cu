@@ -556,12 +556,12 @@ struct SplitPlan {
 constexpr int kSwapRows = 64;   // token rows per unit in the weights-on-M form
 constexpr int kMaxSlots = 4096;
 
-SplitPlan split_plan(int G, int rows_max, int N, int act) {
+SplitPlan split_plan(int G, int rows_max, int N, int act, int max_slots = kMaxSlots) {
   SplitPlan p;
   if (rows_max <= 0 || N % 128 || static_cast<long long>(rows_max) > 64LL * G) return p;
   const long long nonempty = G < rows_max ? G : rows_max;
   const long long units = ((rows_max + kSwapRows - 1) / kSwapRows + nonempty) * (N / 128);
-  const long long cap = units * kMaxSplit < kMaxSlots ? units * kMaxSplit : kMaxSlots;
+  const long long cap = units * kMaxSplit < max_slots ? units * kMaxSplit : max_slots;
   p.unit_cap = static_cast<int>(units);
   p.split_cap = static_cast<int>(cap);
   p.counter_bytes = align_up(static_cast<size_t>(units) * sizeof(int));
@@ -572,7 +572,8 @@ SplitPlan split_plan(int G, int rows_max, int N, int act) {
 
 template <int SWAP, int W, int ACT>
 int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K, void* out,
-               int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream, int* launches) {
+               int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream, int* launches,
+               int max_slots = kMaxSlots) {
   using C = Cfg<SWAP, W, ACT>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -596,7 +597,7 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
                 nullptr, nullptr, 0, 0};
   if (SWAP && ws) {
-    const SplitPlan p = split_plan(G, rows_max, N, ACT);
+    const SplitPlan p = split_plan(G, rows_max, N, ACT, max_slots);
     if (p.bytes && ws_bytes >= p.bytes) {
       args.counters = static_cast<int*>(ws);
       args.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + p.counter_bytes);
@@ -648,6 +649,28 @@ int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, in
     return launch_cfg<0, 128, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
                                  launches);
   return launch_cfg<0, 64, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream, launches);
+}
+
+size_t grouped_gemm_counter_bytes(int G, int rows_max, int N, int act) {
+  return split_plan(G, rows_max, N, act).counter_bytes;
+}
+
+size_t grouped_gemm_ws_bytes_slots(int G, int rows_max, int N, int act, int max_slots) {
+  return split_plan(G, rows_max, N, act, max_slots).bytes;
+}
+
+int grouped_gemm_launch_slots(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
+                              int act, void* out, int* status, void* ws, size_t ws_bytes, int max_slots, int grid_cap,
+                              cudaStream_t stream, int* launches) {
+  if (rows_max == 0) return MOE_OK;
+  if (!grouped_gemm_weights_on_m(G, rows_max, N))
+    return grouped_gemm_launch(a, w, offsets, G, rows_max, N, K, act, out, status, nullptr, 0, grid_cap, stream,
+                               launches);
+  if (act == 1)
+    return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap, stream,
+                                       launches, max_slots);
+  return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap, stream,
+                                     launches, max_slots);
 }
 
 int grouped_gemm_max_groups() { return kMaxGroups; }

@@ -36,9 +36,19 @@ size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act);
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream,
                         int* launches);
+// Bytes at the start of the split-K scratch that hold the ticket counters.
+size_t grouped_gemm_counter_bytes(int G, int rows_max, int N, int act);
+// The same with at most max_slots split-K partial slots (a smaller scratch).
+size_t grouped_gemm_ws_bytes_slots(int G, int rows_max, int N, int act, int max_slots);
+int grouped_gemm_launch_slots(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
+                              int act, void* out, int* status, void* ws, size_t ws_bytes, int max_slots, int grid_cap,
+                              cudaStream_t stream, int* launches);
 int grouped_gemm_max_groups();
 
 int combine_launch(const void* y, const int32_t* inv_perm, const float* topk_w, const void* shared, int T, int H,
                    int k, long long rows_max, void* out, cudaStream_t stream, int* launches);
+
+// Status word and SM count of the current device (first use looks them up).
+int current_device_info(int** status, int* num_sms);
 
 }  // namespace moe

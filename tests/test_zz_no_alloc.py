@@ -1,0 +1,70 @@
+"""moe_grouped_gemm_noalloc: the grouped matmul for callers that cannot
+allocate device memory (its split-K scratch is a fixed array inside the
+library).  Its output must match moe_grouped_gemm's on the same inputs, call
+after call, since every call reuses the same array.
+
+This file is collected last on purpose, so that a run that stops at the first
+failure has already run every other test."""
+import numpy as np
+import pytest
+import torch
+
+from cases import assert_close_layer, to_f64
+from moe_ffn_layer_gb300 import binding as B
+from moe_ffn_layer_gb300 import build as build_mod
+from moe_ffn_layer_gb300 import synth
+from moe_ffn_layer_gb300.layer import bf16_tensor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build_mod.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return B.lib()
+
+
+CASES = [
+    # (rows per group, N, K, act): decode-like groups of a few rows (split-K
+    # runs in the fixed scratch), a down-like shape, and groups too large to split
+    ([1, 2, 0, 1, 3, 1, 0, 2, 1, 1, 4, 0, 1, 2, 1, 1], 768, 2048, 1),
+    ([1, 2, 0, 1, 3, 1, 0, 2, 1, 1, 4, 0, 1, 2, 1, 1], 2048, 768, 0),
+    ([8] * 16, 384, 1024, 1),
+    ([300, 0, 129], 256, 192, 1),
+]
+
+
+@pytest.mark.parametrize("rows,N,K,act", CASES)
+def test_noalloc_matches_grouped_gemm(rows, N, K, act):
+    G = len(rows)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    R = int(off[-1])
+    a = bf16_tensor(synth.random_bf16((R, K), seed=R + K, tag=61), "cuda")
+    w = bf16_tensor(synth.random_bf16((G, 2 * N if act else N, K), seed=N + G, tag=62, sigma=0.03), "cuda")
+    offs = torch.from_numpy(off).cuda()
+    s = torch.cuda.current_stream()
+    nb = B.moe_grouped_gemm_workspace_bytes(G, R, N, K, act)
+    ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+    ref = torch.empty((R, N), dtype=torch.bfloat16, device="cuda")
+    B.moe_grouped_gemm(a, w, offs, G, R, N, K, act, ref, ws, nb, s)
+    ref64 = to_f64(ref)
+    outs = []
+    for _ in range(2):   # two calls in a row on the same fixed scratch
+        out = torch.full((R, N), 3.0, dtype=torch.bfloat16, device="cuda")
+        B.moe_grouped_gemm_noalloc(a, w, offs, G, R, N, K, act, out, s)
+        assert B.moe_last_device_error(s) == 0
+        got = to_f64(out)
+        assert_close_layer(got, ref64, f"noalloc rows={rows} N={N} K={K} act={act}")
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch():
+    """A problem whose split-K scratch would exceed the fixed array is refused
+    before anything is launched (pointers below are never dereferenced)."""
+    fake = 1 << 20
+    with pytest.raises(B.MoEError) as e:
+        B.moe_grouped_gemm_noalloc(fake, fake, fake, 1024, 65536, 262144, 64, 1, fake, None)
+    assert e.value.code == -3
