@@ -243,7 +243,7 @@ def run_gpu(args, w):
         # route and permute calls (the routing statistics come from the GPU path)
         ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
         tw = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
-        rb = B.moe_route_workspace_bytes(w.T, w.E)
+        rb = B.moe_route_workspace_bytes(w.T, w.H, w.E)
         pb = B.moe_permute_workspace_bytes(w.T, w.E)
         rws = torch.empty(max(rb, pb, 256), dtype=torch.uint8, device=dev)
         offs = torch.empty(w.E + 1, dtype=torch.int32, device=dev)

@@ -92,9 +92,14 @@ typedef struct {
  * renormalised over the chosen k).
  *  x        bf16 [T][H];  w_router fp32 [E][H];  bias fp32 [E] or NULL
  *  topk_ids int32 [T][k] (out);  topk_w fp32 [T][k] (out)
- *  ws       scratch of moe_route_workspace_bytes(T, E) bytes (256-B aligned)
+ *  ws       scratch of moe_route_workspace_bytes(T, H, E) bytes (16-byte aligned)
+ * From T = 512 tokens (E and H multiples of 64) the logits are computed on the
+ * tensor cores from an exact three-term bf16 split of the fp32 weights, with
+ * fp32 accumulation; below that, with fp32 FMAs.  Either way the logits carry
+ * fp32 accuracy; expert choices whose logits differ by less than the fp32
+ * summation error can differ from another fp32 evaluation order.
  * Supported: 1 <= k <= min(E, 16), E <= 512, H % 8 == 0. */
-MOE_API size_t moe_route_workspace_bytes(int T, int E);
+MOE_API size_t moe_route_workspace_bytes(int T, int H, int E);
 MOE_API int moe_route(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
               int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, cudaStream_t stream);
 

@@ -36,7 +36,7 @@ class moe_weights(ctypes.Structure):
 
 _P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGS = {
-    "moe_route_workspace_bytes": (_Z, [_I, _I]),
+    "moe_route_workspace_bytes": (_Z, [_I, _I, _I]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_permute_workspace_bytes": (_Z, [_I, _I]),
     "moe_permute": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
@@ -102,8 +102,8 @@ def _check(fn: str, rc: int) -> int:
     return rc
 
 
-def moe_route_workspace_bytes(T: int, E: int) -> int:
-    return lib().moe_route_workspace_bytes(T, E)
+def moe_route_workspace_bytes(T: int, H: int, E: int) -> int:
+    return lib().moe_route_workspace_bytes(T, H, E)
 
 
 def moe_route(x, w_router, bias, T, H, E, k, topk_ids, topk_w, ws, ws_bytes, stream) -> int:

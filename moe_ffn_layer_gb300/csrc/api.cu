@@ -74,7 +74,7 @@ Layout layout(const moe_dims* d, int T) {
                              : 0;
   L.gemm_main = take(L.gemm_main_bytes);
   L.gemm_side = take(L.gemm_side_bytes);
-  L.logits = take(moe::route_ws_bytes(T, d->E));
+  L.logits = take(moe::route_ws_bytes(T, d->H, d->E));
   L.ids = take(Tk * 4);
   L.w = take(Tk * 4);
   L.offsets = take((static_cast<size_t>(d->E) + 1) * 4);
@@ -115,9 +115,9 @@ int current_device_info(int** status, int* num_sms) {
 
 extern "C" {
 
-size_t moe_route_workspace_bytes(int T, int E) {
-  if (T < 0 || E <= 0) return 0;
-  return moe::route_ws_bytes(T, E);
+size_t moe_route_workspace_bytes(int T, int H, int E) {
+  if (T < 0 || H <= 0 || E <= 0) return 0;
+  return moe::route_ws_bytes(T, H, E);
 }
 
 int moe_route(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
@@ -130,10 +130,13 @@ int moe_route(const void* x, const float* w_router, const float* bias, int T, in
   if (!al16(x) || !al16(w_router) || !al16(ws) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
       (reinterpret_cast<uintptr_t>(topk_w) & 3u) || (reinterpret_cast<uintptr_t>(bias) & 3u))
     return MOE_ERR_UNSUPPORTED;
-  if (ws_bytes < moe::route_ws_bytes(T, E)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < moe::route_ws_bytes(T, H, E)) return MOE_ERR_WORKSPACE;
+  DevInfo* di = nullptr;
+  int rc = dev_info(&di);
+  if (rc) return rc;
   int n = 0;
-  const int rc = moe::route_launch(x, w_router, bias, T, H, E, k, topk_ids, topk_w, static_cast<float*>(ws),
-                                   nullptr, stream, &n);
+  rc = moe::route_launch(x, w_router, bias, T, H, E, k, topk_ids, topk_w, static_cast<float*>(ws), nullptr,
+                         di->status, di->sms, stream, &n);
   t_last_launches = n;
   return rc;
 }
@@ -268,10 +271,11 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
   if (T <= moe::route_small_max_tokens()) {
     // decode sizes: router, top-k, counting sort and row gather in one launch
     const moe::DispatchOut dout{offsets, sorted, inv, xperm};
-    rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, &dout, stream, &n);
+    rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, &dout, di->status,
+                           di->sms, stream, &n);
   } else {
-    rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, nullptr, stream,
-                           &n);
+    rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, nullptr,
+                           di->status, di->sms, stream, &n);
     if (!rc)
       rc = moe::permute_launch(ids, x, T, d->H, d->E, d->k, offsets, sorted, inv, xperm, pcounts, di->status,
                                di->sms, stream, &n);

@@ -56,12 +56,12 @@ constexpr int tmem_cols_pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 
 template <int SWAP, int W, int ACT>
 struct Cfg {
   static constexpr int kUnitRows = SWAP ? W : 128;                          // token rows per unit
-  static constexpr int kABytes = SWAP ? (ACT ? 2 : 1) * kTileRows128 : kTileRows128;
+  static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;
   static constexpr int kBBytes = W * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = kSmemBudget / kStageBytes;
-  static constexpr int kOutCols = SWAP ? 128 : (ACT ? W / 2 : W);           // output columns per unit
-  static constexpr int kAccCols = SWAP ? (ACT ? 2 : 1) * W : W;             // TMEM columns per unit
+  static constexpr int kOutCols = SWAP ? 128 : (ACT == 1 ? W / 2 : W);           // output columns per unit
+  static constexpr int kAccCols = SWAP ? (ACT == 1 ? 2 : 1) * W : W;             // TMEM columns per unit
   static constexpr int kNumAcc = 2 * kAccCols <= 512 ? 2 : 1;
   static constexpr int kTmemCols = tmem_cols_pow2(kNumAcc * kAccCols);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256 + 2 * (kMaxGroups + 1) * 4;
@@ -85,11 +85,13 @@ struct GemmArgs {
   float* partials;         // split-K partial accumulators, split_cap slots
   int split_cap;           // sub-units the scratch holds
   int unit_cap;            // units the counters cover
+  int a_kblocks;           // > 0: A has this many K blocks and is re-read for every
+                           // run of them along B's K (tokens-on-M form only)
 };
 
 // fp32 values one TMEM lane keeps per split-K partial
 template <int ACT>
-constexpr int partial_floats() { return (ACT ? 2 : 1) * kSplitRows; }
+constexpr int partial_floats() { return (ACT == 1 ? 2 : 1) * kSplitRows; }
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     nrows = min(rows - rb * C::kUnitRows, C::kUnitRows);
   };
 
-  const int wrows = ACT ? 2 * args.N : args.N;   // weight rows per group
+  const int wrows = ACT == 1 ? 2 * args.N : args.N;   // weight rows per group
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -248,12 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
           if (SWAP) {
             tma_load_2d(sa, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
-            if (ACT) tma_load_2d(sa + kTileRows128, &tm_wgt, &full_bar[stage], kc, wrow + args.N, pol_w);
+            if (ACT == 1) tma_load_2d(sa + kTileRows128, &tm_wgt, &full_bar[stage], kc, wrow + args.N, pol_w);
             for (int j = 0; j < n16; ++j)
               tma_load_2d(sb + j * 16 * kBK * 2, &tm_tok, &full_bar[stage], kc, row0 + 16 * j, pol_tok);
           } else {
-            tma_load_2d(sa, &tm_tok, &full_bar[stage], kc, row0, pol_tok);
-            if (ACT) {
+            const int kca = args.a_kblocks ? (kb % args.a_kblocks) * kBK : kc;
+            tma_load_2d(sa, &tm_tok, &full_bar[stage], kca, row0, pol_tok);
+            if (ACT == 1) {
               tma_load_2d(sb, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
               tma_load_2d(sb + (W / 2) * kBK * 2, &tm_wgt, &full_bar[stage], kc, wrow + args.N, pol_w);
             } else {
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           decode(u, g, row0, nrows, wb);
           const int n16 = (nrows + 15) >> 4;
           idesc = idesc_bf16_f32(128, n16 * 16);
-          chains = swap_chains(n16, C::kAccCols, ACT);
+          chains = swap_chains(n16, C::kAccCols, ACT == 1);
           cw = n16 * 16;
         } else {
           idesc = idesc_bf16_f32(128, W);
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int c = kk & (chains - 1);
               const uint32_t acc = (kb > kb0 || kk >= chains) ? 1u : 0u;
               umma_bf16(d_tmem + c * cw, da + ka, db + ka, idesc, acc);
-              if (ACT) {
+              if (ACT == 1) {
                 const uint64_t du = smem_desc_k128(sa + kTileRows128);
                 umma_bf16(d_tmem + (chains + c) * cw, du + ka, db + ka, idesc, acc);
               }
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // token, chain c of gate (h = 0) / up (h = 1) at column (h*C + c)*cw
         __nv_bfloat16* ocol = args.out + static_cast<size_t>(row0) * args.N + wb * 128 + lrow;
         const int n16 = (nrows + 15) >> 4;
-        const int chains = swap_chains(n16, C::kAccCols, ACT);
+        const int chains = swap_chains(n16, C::kAccCols, ACT == 1);
         const int cw = n16 * 16;
         // sums of the chains for tokens [16j, 16j + 16): gs (gate or plain), us (up)
         auto load_chunk = [&](int j, float (&gs)[16], float (&us)[16]) {
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) gs[i] += __uint_as_float(r[i]);
           }
-          if (ACT) {
+          if (ACT == 1) {
             for (int c = 0; c < chains; ++c) {
               uint32_t r[16];
               tmem_ld_16cols(t_acc + (chains + c) * cw + j * 16, r);
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               if (j * 16 + i < nrows) {
-                const float h = ACT ? gs[i] / (1.0f + __expf(-gs[i])) * us[i] : gs[i];
+                const float h = ACT == 1 ? gs[i] / (1.0f + __expf(-gs[i])) * us[i] : gs[i];
                 ocol[static_cast<size_t>(j * 16 + i) * args.N] = __float2bfloat16_rn(h);
               }
             }
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kSplitRows / 4; ++i) {
             mine[i] = make_float4(gm[4 * i], gm[4 * i + 1], gm[4 * i + 2], gm[4 * i + 3]);
-            if (ACT) mine[kSplitRows / 4 + i] = make_float4(um[4 * i], um[4 * i + 1], um[4 * i + 2], um[4 * i + 3]);
+            if (ACT == 1) mine[kSplitRows / 4 + i] = make_float4(um[4 * i], um[4 * i + 1], um[4 * i + 2], um[4 * i + 3]);
           }
           __threadfence();
           epi_bar_sync();
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < kSplitRows / 4; ++i) {
                   const float4 v = __ldcg(src + i);
                   gs[4 * i] += v.x; gs[4 * i + 1] += v.y; gs[4 * i + 2] += v.z; gs[4 * i + 3] += v.w;
-                  if (ACT) {
+                  if (ACT == 1) {
                     const float4 w4 = __ldcg(src + kSplitRows / 4 + i);
                     us[4 * i] += w4.x; us[4 * i + 1] += w4.y; us[4 * i + 2] += w4.z; us[4 * i + 3] += w4.w;
                   }
@@ -452,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kSplitRows; ++i) {
               if (i < nrows) {
-                const float h = ACT ? gs[i] / (1.0f + __expf(-gs[i])) * us[i] : gs[i];
+                const float h = ACT == 1 ? gs[i] / (1.0f + __expf(-gs[i])) * us[i] : gs[i];
                 ocol[static_cast<size_t>(i) * args.N] = __float2bfloat16_rn(h);
               }
             }
@@ -462,7 +465,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // accumulator row = token row0 + lrow; accumulator column = output column
         const bool live = lrow < nrows;
         __nv_bfloat16* orow = args.out + static_cast<size_t>(row0 + lrow) * args.N + wb * C::kOutCols;
-        if (ACT) {
+        if (ACT == 2) {
+          // fp32 output, no rounding (router logits)
+          float* orow32 = reinterpret_cast<float*>(args.out) + static_cast<size_t>(row0 + lrow) * args.N +
+                          wb * C::kOutCols;
+#pragma unroll 1
+          for (int c = 0; c < W; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32cols(t_acc + c, r);
+            tmem_ld_wait();
+            if (live) {
+              float4* dst = reinterpret_cast<float4*>(orow32 + c);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                     __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+            }
+          }
+        } else if (ACT == 1) {
 #pragma unroll 1
           for (int c = 0; c < W / 2; c += 32) {
             uint32_t gr[32], ur[32];
@@ -573,7 +593,7 @@ SplitPlan split_plan(int G, int rows_max, int N, int act, int max_slots = kMaxSl
 template <int SWAP, int W, int ACT>
 int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K, void* out,
                int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream, int* launches,
-               int max_slots = kMaxSlots) {
+               int max_slots = kMaxSlots, int K_a = 0) {
   using C = Cfg<SWAP, W, ACT>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -585,17 +605,18 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
     if (dev < 64) attr_done[dev] = true;
   }
   CUtensorMap tt, tw;
-  const int wrows = ACT ? 2 * N : N;
+  const int wrows = ACT == 1 ? 2 * N : N;
   const uint32_t tok_box = SWAP ? 16 : 128;
-  const uint32_t wgt_box = SWAP ? 128 : (ACT ? W / 2 : W);
-  if (!make_map(&tt, a, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K), tok_box)) return MOE_ERR_CUDA;
+  const uint32_t wgt_box = SWAP ? 128 : (ACT == 1 ? W / 2 : W);
+  if (!make_map(&tt, a, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K_a ? K_a : K), tok_box))
+    return MOE_ERR_CUDA;
   if (!make_map(&tw, w, static_cast<uint64_t>(G) * wrows, static_cast<uint64_t>(K), wgt_box)) return MOE_ERR_CUDA;
   // upper bound on the unit count: every non-empty group adds at most one partial row block
   const long long nonempty = offsets ? (G < rows_max ? G : rows_max) : 1;
   long long bound =
       (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) * (N / C::kOutCols);
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
-                nullptr, nullptr, 0, 0};
+                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0};
   if (SWAP && ws) {
     const SplitPlan p = split_plan(G, rows_max, N, ACT, max_slots);
     if (p.bytes && ws_bytes >= p.bytes) {
@@ -671,6 +692,22 @@ int grouped_gemm_launch_slots(const void* a, const void* w, const int32_t* offse
                                        launches, max_slots);
   return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap, stream,
                                      launches, max_slots);
+}
+
+int router_gemm_launch(const void* x, const void* wr3, int T, int H, int E, float* logits, int* status, int grid_cap,
+                       cudaStream_t stream, int* launches) {
+  if (T == 0) return MOE_OK;
+  const int K = 3 * H;
+  // narrower N blocks while the row blocks alone would leave SMs idle
+  const long long mtiles = (T + 127) / 128;
+  if (E % 256 == 0 && mtiles * (E / 256) >= grid_cap)
+    return launch_cfg<0, 256, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, 0, grid_cap, stream, launches,
+                                 kMaxSlots, H);
+  if (E % 128 == 0 && mtiles * (E / 128) >= grid_cap)
+    return launch_cfg<0, 128, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, 0, grid_cap, stream, launches,
+                                 kMaxSlots, H);
+  return launch_cfg<0, 64, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, 0, grid_cap, stream, launches,
+                              kMaxSlots, H);
 }
 
 int grouped_gemm_max_groups() { return kMaxGroups; }

@@ -17,12 +17,12 @@ struct DispatchOut {
   void* x_perm;   // may be nullptr
 };
 
-size_t route_ws_bytes(int T, int E);
+size_t route_ws_bytes(int T, int H, int E);
 int route_small_max_tokens();
 // dispatch != nullptr requires T <= route_small_max_tokens().
 int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
-                 int32_t* topk_ids, float* topk_w, float* logits_ws, const DispatchOut* dispatch, cudaStream_t stream,
-                 int* launches);
+                 int32_t* topk_ids, float* topk_w, float* logits_ws, const DispatchOut* dispatch, int* status,
+                 int grid_cap, cudaStream_t stream, int* launches);
 
 size_t permute_ws_bytes(int T, int E);
 int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, int k, int32_t* offsets,
@@ -44,6 +44,11 @@ int grouped_gemm_launch_slots(const void* a, const void* w, const int32_t* offse
                               int act, void* out, int* status, void* ws, size_t ws_bytes, int max_slots, int grid_cap,
                               cudaStream_t stream, int* launches);
 int grouped_gemm_max_groups();
+// logits[T][E] fp32 = x[T][H] . (hi + mid + lo)^T with wr3 = bf16 [E][3H] holding
+// the three bf16 terms of the fp32 router weights in K order (hi | mid | lo);
+// the x tile is re-read for each of the three.  E % 64 == 0, H % 64 == 0.
+int router_gemm_launch(const void* x, const void* wr3, int T, int H, int E, float* logits, int* status, int grid_cap,
+                       cudaStream_t stream, int* launches);
 
 int combine_launch(const void* y, const int32_t* inv_perm, const float* topk_w, const void* shared, int T, int H,
                    int k, long long rows_max, void* out, cudaStream_t stream, int* launches);

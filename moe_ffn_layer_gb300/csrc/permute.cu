@@ -135,27 +135,53 @@ __global__ void __launch_bounds__(kTB)
   for (int e = tl; e < E; e += kTB) block_counts[static_cast<size_t>(blockIdx.x) * E + e] = mask_count(mask, e);
 }
 
-// Large T, pass 2 (one block): block_counts[b][e] -> first row of block b's
-// pairs of expert e; offsets[e] = exclusive scan of the expert totals.
-__global__ void __launch_bounds__(kTB)
+// Large T, pass 2 (one block of kScanThreads): block_counts[b][e] -> first row
+// of block b's pairs of expert e; offsets[e] = exclusive scan of the expert
+// totals.  One warp per expert scans its column of block counts.
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
     permute_scan_kernel(int32_t* __restrict__ block_counts, int B, int E, int32_t* __restrict__ offsets) {
   __shared__ int s_tot[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += kTB) {
+  __shared__ int s_off[kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += kScanThreads / 32) {
     int run = 0;
-    for (int b = 0; b < B; ++b) {
-      const int c = block_counts[static_cast<size_t>(b) * E + e];
-      block_counts[static_cast<size_t>(b) * E + e] = run;
-      run += c;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      const int c = b < B ? block_counts[static_cast<size_t>(b) * E + e] : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (b < B) block_counts[static_cast<size_t>(b) * E + e] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    s_tot[e] = run;
+    if (lane == 0) s_tot[e] = run;
   }
   __syncthreads();
-  const int total = block_exclusive_scan(s_tot, E);
-  for (int e = threadIdx.x; e < E; e += kTB) {
-    offsets[e] = s_tot[e];
-    for (int b = 0; b < B; ++b) block_counts[static_cast<size_t>(b) * E + e] += s_tot[e];
+  if (warp == 0) {   // exclusive scan of the totals over experts
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < E ? s_tot[e] : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (e < E) s_off[e] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) offsets[E] = run;
   }
-  if (threadIdx.x == 0) offsets[E] = total;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kScanThreads) offsets[e] = s_off[e];
+  for (int e = warp; e < E; e += kScanThreads / 32)
+    for (int b = lane; b < B; b += 32) block_counts[static_cast<size_t>(b) * E + e] += s_off[e];
 }
 
 // Large T, pass 3: rows of every pair of the block.
@@ -219,7 +245,7 @@ int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, 
   } else {
     const int B = (T + kTB - 1) / kTB;
     permute_count_kernel<<<B, kTB, 0, stream>>>(topk_ids, T, E, k, block_counts, status);
-    permute_scan_kernel<<<1, kTB, 0, stream>>>(block_counts, B, E, offsets);
+    permute_scan_kernel<<<1, kScanThreads, 0, stream>>>(block_counts, B, E, offsets);
     permute_scatter_kernel<<<B, kTB, 0, stream>>>(topk_ids, T, E, k, block_counts, sorted_token, inv_perm);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     *launches += 3;

@@ -18,8 +18,15 @@
 //             them in slice order, takes the top-k, and (optionally) runs the
 //             counting sort; after a second barrier all CTAs gather the rows.
 //             Decode shapes: one launch instead of four, no global counters.
-//   T >  16   router_tile (fp32 SIMT tile GEMM, 64 tokens x 64 experts per
-//             CTA) then topk_softmax (one warp per token).
+//   T >  16   logits, then topk_softmax (one warp per token; adds the bias).
+//             Logits for T >= 512 (E, H multiples of 64) come from the tensor
+//             cores: each fp32 weight is split exactly into three bf16 terms
+//             w = hi + mid + lo (hi = bf16(w), mid = bf16(w - hi), lo =
+//             bf16(w - hi - mid); every subtraction is exact in fp32 and the
+//             three terms carry the full 24-bit significand), and since x is
+//             bf16 every product x*term is exact in fp32; the grouped GEMM
+//             adds them in fp32 with K = 3H.  Other sizes: router_tile, an fp32
+//             SIMT tile GEMM, 64 tokens x 64 experts per CTA.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -35,13 +42,13 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
-// fp32 SIMT GEMM: logits[T][E] = x[T][H] . Wr[E][H]^T (+ b).  CTA tile 64 x 64,
+// fp32 SIMT GEMM: logits[T][E] = x[T][H] . Wr[E][H]^T.  CTA tile 64 x 64,
 // K chunk 32, 256 threads each owning a 4 x 4 block of outputs.
 constexpr int kRT = 64, kRE = 64, kRK = 32;
 
 __global__ void __launch_bounds__(256)
-    router_tile_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr,
-                       const float* __restrict__ bias, int T, int H, int E, float* __restrict__ logits) {
+    router_tile_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, int T, int H, int E,
+                       float* __restrict__ logits) {
   __shared__ float xs[kRK][kRT + 4];
   __shared__ float ws[kRK][kRE + 4];
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE;
@@ -87,7 +94,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + tx * 4 + j;
-      if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
+      if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j];
     }
   }
 }
@@ -97,24 +104,54 @@ __global__ void __launch_bounds__(256)
 // winner stays in lane r.  The chosen ids are then ranked by id across lanes
 // (ascending order), and w_j = exp(l_j - max) / sum_i exp(l_i - max) over the
 // chosen k, the sum taken by a fixed butterfly.  Registers only.
+//
+// Refinement (logits from the tensor cores, refine != nullptr): if the k-th
+// and (k+1)-th logits lie within kRefineDelta, every expert whose logit lies
+// within kRefineDelta of the k-th is re-evaluated with fp32 FMAs (x . Wr[e] +
+// b[e]) and the selection is run again.  The tensor-core logits differ from
+// fp32 ones by far less than kRefineDelta / 2, so experts outside that band
+// keep their side of the boundary and the choice equals the fp32 choice.
 constexpr int kTopkMaxPerLane = kMaxExperts / 32;
+constexpr float kRefineDelta = 1e-3f;
 
-__device__ void warp_topk_softmax(const float* l, int E, int k, int32_t* ids_out, float* w_out) {
+struct Refine {
+  const __nv_bfloat16* x;   // this token's row [H]
+  const float* wr;          // [E][H]
+  int H;
+};
+
+__device__ __forceinline__ float warp_dot_fp32(const __nv_bfloat16* x, const float* w, int H) {
   const int lane = threadIdx.x & 31;
-  float v[kTopkMaxPerLane];
-#pragma unroll
-  for (int i = 0; i < kTopkMaxPerLane; ++i) {
-    const int e = i * 32 + lane;
-    v[i] = e < E ? l[e] : -INFINITY;
+  float acc = 0.f;
+  for (int h0 = lane * 8; h0 < H; h0 += 256) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(x + h0);
+    const float4 w0 = *reinterpret_cast<const float4*>(w + h0);
+    const float4 w1 = *reinterpret_cast<const float4*>(w + h0 + 4);
+    float f[8];
+    bf16x8_to_f32(xv, f);
+    acc = fmaf(f[0], w0.x, acc); acc = fmaf(f[1], w0.y, acc); acc = fmaf(f[2], w0.z, acc); acc = fmaf(f[3], w0.w, acc);
+    acc = fmaf(f[4], w1.x, acc); acc = fmaf(f[5], w1.y, acc); acc = fmaf(f[6], w1.z, acc); acc = fmaf(f[7], w1.w, acc);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
+}
+
+// k rounds of arg-max over v (lane-strided, E entries); returns this lane's
+// round winner (lane r keeps round r) and the value of round `extra` (-inf if none).
+template <int NPL>
+__device__ __forceinline__ void warp_select(const float (&v)[NPL], int E, int rounds, int& my_id, float& my_v,
+                                            float& last_v) {
+  const int lane = threadIdx.x & 31;
   uint32_t taken = 0;   // bit i: element i of this lane already chosen
-  int my_id = 0x7fffffff;
-  float my_v = -INFINITY;
-  for (int r = 0; r < k; ++r) {
+  my_id = 0x7fffffff;
+  my_v = -INFINITY;
+  last_v = -INFINITY;
+  for (int r = 0; r < rounds; ++r) {
     float best = -INFINITY;
     int bid = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < kTopkMaxPerLane; ++i) {
+    for (int i = 0; i < NPL; ++i) {
       const int e = i * 32 + lane;
       if (e < E && !(taken >> i & 1u) && (v[i] > best || (v[i] == best && e < bid))) { best = v[i]; bid = e; }
     }
@@ -125,8 +162,45 @@ __device__ void warp_topk_softmax(const float* l, int E, int k, int32_t* ids_out
       if (ob > best || (ob == best && oi < bid)) { best = ob; bid = oi; }
     }
     if (lane == r) { my_id = bid; my_v = best; }
+    last_v = best;
     if (bid < E && (bid & 31) == lane) taken |= 1u << (bid >> 5);
   }
+}
+
+// NPL = logits per lane (E <= 32 * NPL).
+template <int NPL>
+__device__ void warp_topk_softmax(const float* l, const float* bias, int E, int k, int32_t* ids_out, float* w_out,
+                                  const Refine* refine = nullptr) {
+  const int lane = threadIdx.x & 31;
+  float v[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = i * 32 + lane;
+    v[i] = e < E ? l[e] + (bias ? bias[e] : 0.f) : -INFINITY;
+  }
+  int my_id;
+  float my_v, last_v;
+  if (refine && k < E) {
+    warp_select(v, E, k + 1, my_id, my_v, last_v);   // round k holds the (k+1)-th value
+    const float vk = __shfl_sync(0xffffffffu, my_v, k - 1);
+    if (vk - last_v < kRefineDelta) {
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int e0 = i * 32;
+        if (e0 >= E) break;
+        uint32_t band = __ballot_sync(0xffffffffu, e0 + lane < E && fabsf(v[i] - vk) <= kRefineDelta);
+        while (band) {
+          const int src = __ffs(band) - 1;
+          band &= band - 1;
+          const int e = e0 + src;
+          const float exact = warp_dot_fp32(refine->x, refine->wr + static_cast<size_t>(e) * refine->H, refine->H) +
+                              (bias ? bias[e] : 0.f);
+          if (lane == src) v[i] = exact;
+        }
+      }
+    }
+  }
+  warp_select(v, E, k, my_id, my_v, last_v);
   // position of this lane's id among the chosen ids
   int rank = 0;
   for (int j = 0; j < k; ++j) rank += __shfl_sync(0xffffffffu, my_id, j) < my_id ? 1 : 0;
@@ -141,13 +215,37 @@ __device__ void warp_topk_softmax(const float* l, int E, int k, int32_t* ids_out
   }
 }
 
+// refine_wr != nullptr: the logits came from the tensor cores; near ties are
+// re-evaluated in fp32 from x and Wr (see warp_topk_softmax).
+template <int NPL>
 __global__ void __launch_bounds__(256)
-    topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
-                        float* __restrict__ topk_w) {
+    topk_softmax_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+                        int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+                        const __nv_bfloat16* __restrict__ x, const float* __restrict__ refine_wr, int H) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  warp_topk_softmax(logits + static_cast<size_t>(t) * E, E, k, topk_ids + static_cast<size_t>(t) * k,
-                    topk_w + static_cast<size_t>(t) * k);
+  const Refine r{x + static_cast<size_t>(t) * H, refine_wr, H};
+  warp_topk_softmax<NPL>(logits + static_cast<size_t>(t) * E, bias, E, k, topk_ids + static_cast<size_t>(t) * k,
+                         topk_w + static_cast<size_t>(t) * k, refine_wr ? &r : nullptr);
+}
+
+// wr3[e][j*H + h] = j-th bf16 term of Wr[e][h] (j = 0 hi, 1 mid, 2 lo).
+__global__ void __launch_bounds__(256)
+    split_router_weights_kernel(const float* __restrict__ wr, int E, int H, __nv_bfloat16* __restrict__ wr3) {
+  const size_t n = static_cast<size_t>(E) * H;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t e = i / H, h = i - e * H;
+    const float w = wr[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    __nv_bfloat16* row = wr3 + e * 3 * static_cast<size_t>(H);
+    row[h] = hi;
+    row[H + h] = mid;
+    row[2 * static_cast<size_t>(H) + h] = __float2bfloat16_rn(r2);
+  }
 }
 
 // ---------------------------------------------------------------- T <= 16: one cluster
@@ -170,6 +268,7 @@ struct SmallArgs {
   __nv_bfloat16* x_perm;      // nullptr: no row gather
 };
 
+template <int NPL>
 __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kSmallThreads, 1)
     route_small_kernel(const SmallArgs a) {
   __shared__ float part[kSmallT * kMaxExperts];   // [S][T][E]; S * E <= max(256, E)
@@ -229,7 +328,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kSmallThr
       part[i] = v;
     }
     __syncthreads();
-    if (warp < T) warp_topk_softmax(part + warp * E, E, k, s_ids + warp * k, s_w + warp * k);
+    if (warp < T) warp_topk_softmax<NPL>(part + warp * E, nullptr, E, k, s_ids + warp * k, s_w + warp * k);
     __syncthreads();
     for (int i = threadIdx.x; i < T * k; i += kSmallThreads) {
       a.topk_ids[i] = s_ids[i];
@@ -284,13 +383,21 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kSmallThr
 
 }  // namespace
 
-size_t route_ws_bytes(int T, int E) { return align_up(static_cast<size_t>(T) * E * sizeof(float)); }
+constexpr int kTcMinT = 512;   // from this many tokens the logits come from the tensor cores
+
+bool route_uses_tc(int T, int H, int E) { return T >= kTcMinT && E % 64 == 0 && H % 64 == 0; }
+
+size_t route_ws_bytes(int T, int H, int E) {
+  size_t b = align_up(static_cast<size_t>(T) * E * sizeof(float));
+  if (route_uses_tc(T, H, E)) b += align_up(static_cast<size_t>(E) * 3 * H * 2);
+  return b;
+}
 
 int route_small_max_tokens() { return kSmallT; }
 
 int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
-                 int32_t* topk_ids, float* topk_w, float* logits_ws, const DispatchOut* dispatch, cudaStream_t stream,
-                 int* launches) {
+                 int32_t* topk_ids, float* topk_w, float* logits_ws, const DispatchOut* dispatch, int* status,
+                 int grid_cap, cudaStream_t stream, int* launches) {
   if (T == 0) return MOE_OK;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (T <= kSmallT) {
@@ -304,16 +411,40 @@ int route_launch(const void* x, const float* w_router, const float* bias, int T,
       a.inv_perm = dispatch->inv_perm;
       a.x_perm = static_cast<__nv_bfloat16*>(dispatch->x_perm);
     }
-    route_small_kernel<<<kClusterCtas, kSmallThreads, 0, stream>>>(a);
+    if (E <= 128)
+      route_small_kernel<4><<<kClusterCtas, kSmallThreads, 0, stream>>>(a);
+    else if (E <= 256)
+      route_small_kernel<8><<<kClusterCtas, kSmallThreads, 0, stream>>>(a);
+    else
+      route_small_kernel<16><<<kClusterCtas, kSmallThreads, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     ++*launches;
     return MOE_OK;
   }
-  dim3 grid((T + kRT - 1) / kRT, (E + kRE - 1) / kRE);
-  router_tile_kernel<<<grid, 256, 0, stream>>>(xb, w_router, bias, T, H, E, logits_ws);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  ++*launches;
-  topk_softmax_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits_ws, T, E, k, topk_ids, topk_w);
+  if (route_uses_tc(T, H, E)) {
+    __nv_bfloat16* wr3 = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(logits_ws) +
+                                                          align_up(static_cast<size_t>(T) * E * sizeof(float)));
+    const size_t n = static_cast<size_t>(E) * H;
+    split_router_weights_kernel<<<static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, stream>>>(
+        w_router, E, H, wr3);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    ++*launches;
+    const int rc = router_gemm_launch(x, wr3, T, H, E, logits_ws, status, grid_cap, stream, launches);
+    if (rc) return rc;
+  } else {
+    dim3 grid((T + kRT - 1) / kRT, (E + kRE - 1) / kRE);
+    router_tile_kernel<<<grid, 256, 0, stream>>>(xb, w_router, T, H, E, logits_ws);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    ++*launches;
+  }
+  const float* rw = route_uses_tc(T, H, E) ? w_router : nullptr;
+  const int tg = (T + 7) / 8;
+  if (E <= 128)
+    topk_softmax_kernel<4><<<tg, 256, 0, stream>>>(logits_ws, bias, T, E, k, topk_ids, topk_w, xb, rw, H);
+  else if (E <= 256)
+    topk_softmax_kernel<8><<<tg, 256, 0, stream>>>(logits_ws, bias, T, E, k, topk_ids, topk_w, xb, rw, H);
+  else
+    topk_softmax_kernel<16><<<tg, 256, 0, stream>>>(logits_ws, bias, T, E, k, topk_ids, topk_w, xb, rw, H);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;

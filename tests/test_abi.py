@@ -52,7 +52,7 @@ def test_workspace_queries(lib):
     assert big >= Tk * (2048 + 768 + 2048) * 2
     assert big % 256 == 0
     assert B.moe_workspace_bytes(B.moe_dims(2048, 128, 8, 700, 2048), 1) == 0   # I % 64 != 0
-    assert B.moe_route_workspace_bytes(16, 128) >= 16 * 128 * 4
+    assert B.moe_route_workspace_bytes(16, 2048, 128) >= 16 * 128 * 4
     assert B.moe_permute_workspace_bytes(256, 128) == 0          # one-block path needs none
     assert B.moe_permute_workspace_bytes(4096, 128) >= 16 * 128 * 4
     # split-K scratch only for the weights-on-M form (few rows per group)

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from cases import (ROUTE_W_ATOL, assert_close_layer, inputs, layer, routing, to_f64, x_tensor)
+from cases import (assert_close_layer, inputs, layer, route_w_atol, routing, to_f64, x_tensor)
 from moe_ffn_layer_gb300 import binding as B
 from moe_ffn_layer_gb300 import build as build_mod
 from moe_ffn_layer_gb300 import synth
@@ -61,30 +61,61 @@ def test_route(name, T):
     b = None if inp["bias"] is None else f32(inp["bias"])
     ids = torch.empty((T, w.k), dtype=torch.int32, device="cuda")
     tw = torch.empty((T, w.k), dtype=torch.float32, device="cuda")
-    nb = B.moe_route_workspace_bytes(T, w.E)
+    nb = B.moe_route_workspace_bytes(T, w.H, w.E)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
     B.moe_route(x, wr, b, T, w.H, w.E, w.k, ids, tw, ws, nb, stream())
     no_device_error()
     np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
-    np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=0, atol=ROUTE_W_ATOL)
+    np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=0, atol=route_w_atol(T, w.H, w.E))
 
 
 @pytest.mark.parametrize("T,H,E,k", [(1, 256, 8, 2), (5, 520, 8, 3), (16, 2048, 64, 6), (16, 512, 512, 16),
-                                     (3, 4096, 256, 8), (17, 256, 40, 4)])
+                                     (3, 4096, 256, 8), (17, 256, 40, 4), (511, 256, 64, 4), (512, 256, 64, 4),
+                                     (700, 192, 512, 16), (1000, 128, 40, 3)])
 def test_route_shapes(T, H, E, k):
     """The one-cluster router (T <= 16) across slice counts, E up to 512 and
-    k up to 16, and the tiled router just above it."""
+    k up to 16, the fp32 tiled router, and the tensor-core router (three-term
+    bf16 split of the fp32 weights) from T = 512 on, with a ragged last tile."""
     w = synth.Workload("r", T, H, E, k, 64, 0, sigma_router=0.3, zipf_s=1.0)
     x_np, wr_np, b_np = synth.make_activations(w, 4)
     ids_ref, w_ref, _ = om.route(x_np, wr_np, b_np, k)
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
     tw = torch.empty((T, k), dtype=torch.float32, device="cuda")
-    nb = B.moe_route_workspace_bytes(T, E)
+    nb = B.moe_route_workspace_bytes(T, H, E)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
     B.moe_route(bf16_tensor(x_np, "cuda"), f32(wr_np), f32(b_np), T, H, E, k, ids, tw, ws, nb, stream())
     no_device_error()
     np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
-    np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=0, atol=ROUTE_W_ATOL)
+    np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=0, atol=route_w_atol(T, H, E))
+
+
+def test_route_near_ties_tensor_core_path():
+    """Experts with nearly equal router rows: most tokens have a k-th vs
+    (k+1)-th logit gap below 1e-3, so the tensor-core router re-evaluates
+    the band around the boundary in fp32; the ids must equal the oracle's.
+    Tokens whose fp64 gap is below 2e-4 are dropped (closer calls depend on
+    the fp32 summation order itself)."""
+    H, E, k = 256, 64, 4
+    rng = np.random.default_rng(21)
+    x_bits = synth.random_bf16((4096, H), seed=21, tag=70)
+    base = rng.standard_normal(H).astype(np.float32) * 0.1
+    wr = (base[None, :] + 4e-4 * rng.standard_normal((E, H))).astype(np.float32)
+    l64 = om.bf16_to_f64(x_bits) @ wr.astype(np.float64).T
+    srt = np.sort(l64, axis=1)[:, ::-1]
+    gap = srt[:, k - 1] - srt[:, k]
+    keep = np.nonzero(gap > 2e-4)[0][:2048]
+    assert len(keep) >= 1024 and np.mean(gap[keep] < 1e-3) > 0.5
+    x_np = np.ascontiguousarray(x_bits[keep])
+    T = len(keep)
+    ids_ref, w_ref, _ = om.route(x_np, wr, None, k)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    tw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    nb = B.moe_route_workspace_bytes(T, H, E)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    B.moe_route(bf16_tensor(x_np, "cuda"), f32(wr), None, T, H, E, k, ids, tw, ws, nb, stream())
+    no_device_error()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(tw.cpu().numpy(), w_ref, rtol=0, atol=route_w_atol(T, H, E))
 
 
 # ---------------------------------------------------------------- a2 permute
