@@ -137,13 +137,22 @@ def barrier(world):
 
 
 def max_over_ranks(v: float, world: int) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job(ms_local: float, tokens_per_rank: int, steps: int, world: int):
+    """(tokens/s of all ranks together, ms of the slowest rank) for `steps`
+    timed steps of `tokens_per_rank` tokens on every rank."""
+    ms = max_over_ranks(ms_local, world)
+    return world * steps * tokens_per_rank / (ms / 1e3), ms
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -233,9 +242,8 @@ def run_gpu(args, w):
     clocks = clk.stop() if clk else None
     barrier(world)
     ms_local = e0.elapsed_time(e1)
-    ms = max_over_ranks(ms_local, world)
+    value, ms = whole_job(ms_local, w.T, K, world)
     assert B.moe_last_device_error(stream) == 0
-    value = world * K * w.T / (ms / 1e3)
 
     result = None
     if rank == 0:
