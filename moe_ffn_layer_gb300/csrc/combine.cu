@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kCombineThreads)
                    long long rows_max, uint4* __restrict__ out) {
   __shared__ int s_row[kMaxTopK];
   __shared__ float s_w[kMaxTopK];
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int t = blockIdx.x;
   if (threadIdx.x < k) {
     const int r = inv_perm[static_cast<size_t>(t) * k + threadIdx.x];
@@ -59,10 +61,10 @@ __global__ void __launch_bounds__(kCombineThreads)
 int combine_launch(const void* y, const int32_t* inv_perm, const float* topk_w, const void* shared, int T, int H,
                    int k, long long rows_max, void* out, cudaStream_t stream, int* launches) {
   if (T == 0) return MOE_OK;
-  combine_kernel<<<T, kCombineThreads, 0, stream>>>(static_cast<const uint4*>(y), inv_perm, topk_w,
-                                                    static_cast<const uint4*>(shared), T, H, k, rows_max,
-                                                    static_cast<uint4*>(out));
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_chained(combine_kernel, dim3(T), dim3(kCombineThreads), 0, stream, static_cast<const uint4*>(y), inv_perm,
+                     topk_w, static_cast<const uint4*>(shared), T, H, k, rows_max,
+                     static_cast<uint4*>(out)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
 }

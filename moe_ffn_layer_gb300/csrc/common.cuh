@@ -35,6 +35,38 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---------------------------------------------------------------- launch chaining
+// Programmatic dependent launch: a kernel launched with launch_chained() may
+// start while the previous kernel of its stream is still running; it must call
+// chain_wait() before its first global-memory access (the wait returns once
+// the previous grid has completed and its writes are visible), and calls
+// chain_release() to let the next kernel of the stream start its own launch.
+// Without the launch attribute both are no-ops.
+__device__ __forceinline__ void chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void chain_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Releases the next kernel when the thread leaves the scope (its work done):
+// the next kernel's CTAs then take SMs only as this kernel's CTAs finish, and
+// never sit on SMs that a kernel of another stream could use meanwhile.
+struct ChainReleaseAtExit {
+  __device__ ~ChainReleaseAtExit() { chain_release(); }
+};
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -129,15 +129,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = args.G;
   const int NB = args.N / C::kOutCols;   // weight blocks per group
 
-  // ---- group offsets into shared memory (all threads), barriers (warp 1)
-  for (int i = threadIdx.x; i <= G; i += kThreads)
-    s_off[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows_max);
+  // ---- prologue (may overlap the previous kernel of the stream): barriers,
+  // tensor-map prefetch; then wait for that kernel's writes
   if (warp == 1 && lane == 0) {
     for (int s = 0; s < C::kStages; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
     mbar_init(done_bar, 1);
     fence_barrier_init();
+  } else if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_tok);
+    tma_prefetch_desc(&tm_wgt);
   }
+  chain_wait();
+  const ChainReleaseAtExit release_next;
+  // ---- group offsets into shared memory (all threads)
+  for (int i = threadIdx.x; i <= G; i += kThreads)
+    s_off[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows_max);
   __syncthreads();
   const int kblocks = args.K / kBK;
   // ---- unit table (warp 0): checks, unit prefix per group, split choice
@@ -186,8 +193,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       *s_total = any_bad ? 0 : units * S;
       *abort_flag = 0;
       if (any_bad && blockIdx.x == 0) set_status(args.status, MOE_ERR_DEVICE_CHECK);
-      tma_prefetch_desc(&tm_tok);
-      tma_prefetch_desc(&tm_wgt);
     }
   }
   __syncthreads();
@@ -629,8 +634,9 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   }
   int grid = static_cast<int>(bound < grid_cap ? bound : grid_cap);
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<SWAP, W, ACT><<<grid, kThreads, C::kSmemBytes, stream>>>(tt, tw, args);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_chained(grouped_gemm_kernel<SWAP, W, ACT>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, tt, tw,
+                     args) != cudaSuccess)
+    return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
 }

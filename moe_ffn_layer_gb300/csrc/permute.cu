@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(kTB)
                          int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_perm, int* status) {
   __shared__ uint32_t mask[kMaxExperts * kMaskWords];
   __shared__ int s_off[kMaxExperts];
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int t = threadIdx.x;
   for (int i = t; i < E * kMaskWords; i += kTB) mask[i] = 0;
   __syncthreads();
@@ -127,6 +129,8 @@ __global__ void __launch_bounds__(kTB)
     permute_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ block_counts,
                          int* status) {
   __shared__ uint32_t mask[kMaxExperts * kMaskWords];
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int tl = threadIdx.x, t = blockIdx.x * kTB + tl;
   for (int i = tl; i < E * kMaskWords; i += kTB) mask[i] = 0;
   __syncthreads();
@@ -144,6 +148,8 @@ __global__ void __launch_bounds__(kScanThreads)
     permute_scan_kernel(int32_t* __restrict__ block_counts, int B, int E, int32_t* __restrict__ offsets) {
   __shared__ int s_tot[kMaxExperts];
   __shared__ int s_off[kMaxExperts];
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = warp; e < E; e += kScanThreads / 32) {
     int run = 0;
@@ -190,6 +196,8 @@ __global__ void __launch_bounds__(kTB)
                            const int32_t* __restrict__ block_base, int32_t* __restrict__ sorted_token,
                            int32_t* __restrict__ inv_perm) {
   __shared__ uint32_t mask[kMaxExperts * kMaskWords];
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int tl = threadIdx.x, t = blockIdx.x * kTB + tl;
   for (int i = tl; i < E * kMaskWords; i += kTB) mask[i] = 0;
   __syncthreads();
@@ -215,6 +223,8 @@ __global__ void __launch_bounds__(kTB)
 __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_token,
                        const int32_t* __restrict__ offsets, int E, int T, int H, uint4* __restrict__ x_perm) {
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int rows = offsets[E];
   const int vec = H / 8;
   const int lane = threadIdx.x & 31;
@@ -239,24 +249,29 @@ int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, 
                    int num_sms, cudaStream_t stream, int* launches) {
   if (T == 0) return MOE_OK;
   if (T <= kTB) {
-    permute_small_kernel<<<1, kTB, 0, stream>>>(topk_ids, T, E, k, offsets, sorted_token, inv_perm, status);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_chained(permute_small_kernel, dim3(1), dim3(kTB), 0, stream, topk_ids, T, E, k, offsets, sorted_token,
+                       inv_perm, status) != cudaSuccess)
+      return MOE_ERR_CUDA;
     ++*launches;
   } else {
     const int B = (T + kTB - 1) / kTB;
-    permute_count_kernel<<<B, kTB, 0, stream>>>(topk_ids, T, E, k, block_counts, status);
-    permute_scan_kernel<<<1, kScanThreads, 0, stream>>>(block_counts, B, E, offsets);
-    permute_scatter_kernel<<<B, kTB, 0, stream>>>(topk_ids, T, E, k, block_counts, sorted_token, inv_perm);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_chained(permute_count_kernel, dim3(B), dim3(kTB), 0, stream, topk_ids, T, E, k, block_counts,
+                       status) != cudaSuccess ||
+        launch_chained(permute_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, block_counts, B, E, offsets) !=
+            cudaSuccess ||
+        launch_chained(permute_scatter_kernel, dim3(B), dim3(kTB), 0, stream, topk_ids, T, E, k,
+                       static_cast<const int32_t*>(block_counts), sorted_token, inv_perm) != cudaSuccess)
+      return MOE_ERR_CUDA;
     *launches += 3;
   }
   if (x_perm) {
     const long long rows = static_cast<long long>(T) * k;
     long long grid = (rows + 7) / 8;
     if (grid > 8LL * num_sms) grid = 8LL * num_sms;
-    gather_rows_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
-        static_cast<const uint4*>(x), sorted_token, offsets, E, T, H, static_cast<uint4*>(x_perm));
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_chained(gather_rows_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, stream,
+                       static_cast<const uint4*>(x), static_cast<const int32_t*>(sorted_token),
+                       static_cast<const int32_t*>(offsets), E, T, H, static_cast<uint4*>(x_perm)) != cudaSuccess)
+      return MOE_ERR_CUDA;
     ++*launches;
   }
   return MOE_OK;

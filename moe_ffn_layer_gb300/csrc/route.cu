@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(256)
                        float* __restrict__ logits) {
   __shared__ float xs[kRK][kRT + 4];
   __shared__ float ws[kRK][kRE + 4];
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE;
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;   // 16 x 16 threads
@@ -222,6 +224,8 @@ __global__ void __launch_bounds__(256)
     topk_softmax_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
                         int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
                         const __nv_bfloat16* __restrict__ x, const float* __restrict__ refine_wr, int H) {
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   const Refine r{x + static_cast<size_t>(t) * H, refine_wr, H};
@@ -232,6 +236,8 @@ __global__ void __launch_bounds__(256)
 // wr3[e][j*H + h] = j-th bf16 term of Wr[e][h] (j = 0 hi, 1 mid, 2 lo).
 __global__ void __launch_bounds__(256)
     split_router_weights_kernel(const float* __restrict__ wr, int E, int H, __nv_bfloat16* __restrict__ wr3) {
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const size_t n = static_cast<size_t>(E) * H;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -277,6 +283,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kSmallThr
   __shared__ uint32_t s_mask[kMaxExperts];
   __shared__ int s_off[kMaxExperts];
   cg::cluster_group cluster = cg::this_cluster();
+  chain_wait();
+  const ChainReleaseAtExit release_next;
   const int rank = static_cast<int>(cluster.block_rank());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, E = a.E, k = a.k, S = a.S;
@@ -411,13 +419,14 @@ int route_launch(const void* x, const float* w_router, const float* bias, int T,
       a.inv_perm = dispatch->inv_perm;
       a.x_perm = static_cast<__nv_bfloat16*>(dispatch->x_perm);
     }
+    cudaError_t rc;
     if (E <= 128)
-      route_small_kernel<4><<<kClusterCtas, kSmallThreads, 0, stream>>>(a);
+      rc = launch_chained(route_small_kernel<4>, dim3(kClusterCtas), dim3(kSmallThreads), 0, stream, a);
     else if (E <= 256)
-      route_small_kernel<8><<<kClusterCtas, kSmallThreads, 0, stream>>>(a);
+      rc = launch_chained(route_small_kernel<8>, dim3(kClusterCtas), dim3(kSmallThreads), 0, stream, a);
     else
-      route_small_kernel<16><<<kClusterCtas, kSmallThreads, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+      rc = launch_chained(route_small_kernel<16>, dim3(kClusterCtas), dim3(kSmallThreads), 0, stream, a);
+    if (rc != cudaSuccess) return MOE_ERR_CUDA;
     ++*launches;
     return MOE_OK;
   }
@@ -425,27 +434,31 @@ int route_launch(const void* x, const float* w_router, const float* bias, int T,
     __nv_bfloat16* wr3 = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(logits_ws) +
                                                           align_up(static_cast<size_t>(T) * E * sizeof(float)));
     const size_t n = static_cast<size_t>(E) * H;
-    split_router_weights_kernel<<<static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096), 256, 0, stream>>>(
-        w_router, E, H, wr3);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_chained(split_router_weights_kernel, dim3(static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096)),
+                       dim3(256), 0, stream, w_router, E, H, wr3) != cudaSuccess)
+      return MOE_ERR_CUDA;
     ++*launches;
     const int rc = router_gemm_launch(x, wr3, T, H, E, logits_ws, status, grid_cap, stream, launches);
     if (rc) return rc;
   } else {
     dim3 grid((T + kRT - 1) / kRT, (E + kRE - 1) / kRE);
-    router_tile_kernel<<<grid, 256, 0, stream>>>(xb, w_router, T, H, E, logits_ws);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_chained(router_tile_kernel, grid, dim3(256), 0, stream, xb, w_router, T, H, E, logits_ws) != cudaSuccess)
+      return MOE_ERR_CUDA;
     ++*launches;
   }
   const float* rw = route_uses_tc(T, H, E) ? w_router : nullptr;
   const int tg = (T + 7) / 8;
+  cudaError_t rc;
   if (E <= 128)
-    topk_softmax_kernel<4><<<tg, 256, 0, stream>>>(logits_ws, bias, T, E, k, topk_ids, topk_w, xb, rw, H);
+    rc = launch_chained(topk_softmax_kernel<4>, dim3(tg), dim3(256), 0, stream, static_cast<const float*>(logits_ws),
+                        bias, T, E, k, topk_ids, topk_w, xb, rw, H);
   else if (E <= 256)
-    topk_softmax_kernel<8><<<tg, 256, 0, stream>>>(logits_ws, bias, T, E, k, topk_ids, topk_w, xb, rw, H);
+    rc = launch_chained(topk_softmax_kernel<8>, dim3(tg), dim3(256), 0, stream, static_cast<const float*>(logits_ws),
+                        bias, T, E, k, topk_ids, topk_w, xb, rw, H);
   else
-    topk_softmax_kernel<16><<<tg, 256, 0, stream>>>(logits_ws, bias, T, E, k, topk_ids, topk_w, xb, rw, H);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    rc = launch_chained(topk_softmax_kernel<16>, dim3(tg), dim3(256), 0, stream, static_cast<const float*>(logits_ws),
+                        bias, T, E, k, topk_ids, topk_w, xb, rw, H);
+  if (rc != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
 }
