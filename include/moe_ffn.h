@@ -134,8 +134,9 @@ MOE_API int moe_permute(const int32_t* topk_ids, const void* x, int T, int H, in
  *                again (after a device error, zero it again).  Calls that share
  *                a scratch buffer must not overlap on the GPU.
  * bf16 inputs, fp32 accumulation in tensor memory, bf16 (round-to-nearest)
- * output.  Split-K (only for groups of at most 16 rows, weights-on-M form)
- * adds fp32 partials in a fixed order: results do not depend on scheduling.
+ * output.  With scratch, launches whose groups have at most 16 rows may cut a
+ * unit's K range between CTAs (S-way split or stream-K); the partial sums are
+ * added in a fixed order, so results do not depend on scheduling.
  * Supported: K % 64 == 0, N % 64 == 0, G <= 1024. */
 MOE_API size_t moe_grouped_gemm_workspace_bytes(int G, int rows_max, int N, int K, int act);
 MOE_API int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max, int N,

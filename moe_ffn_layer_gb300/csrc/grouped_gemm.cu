@@ -29,14 +29,14 @@
 // weight block, row block) so that CTAs running side by side share a weight
 // block in L2.
 //
-// Split-K (weights-on-M form, every group <= 16 rows, scratch given): when the
-// units do not spread evenly over the grid, every CTA picks the same split S
-// in {1, 2, 4, 8} from the unit count; sub-unit (u, s) covers K blocks
-// [s*KB/S, (s+1)*KB/S).  Each sub-unit stores its fp32 partial accumulator,
-// then takes a ticket on the unit's counter; the ticket holder that arrives
-// last adds the S partials in split order (its own from registers), resets the
-// counter to zero and runs the epilogue.  The result does not depend on which
-// CTA arrives last, and no CTA waits for another.
+// Stream-K (weights-on-M form, every group <= 16 rows, scratch given): when
+// whole units do not spread evenly over the grid, the units' K blocks are laid
+// end to end and every CTA takes an equal contiguous share.  A unit cut
+// between CTAs becomes pieces; each piece stores its fp32 partial accumulator
+// and takes a ticket on the unit's counter; the ticket holder that arrives
+// last adds the pieces' partials in piece order, resets the counter to zero
+// and runs the epilogue.  The result does not depend on which CTA arrives
+// last, and no CTA waits for another.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -103,6 +103,67 @@ __host__ __device__ constexpr int swap_chains(int n16, int acc_cols, int act) {
   return 4 * (act ? 2 : 1) * n16 * 16 <= acc_cols ? 4 : (2 * (act ? 2 : 1) * n16 * 16 <= acc_cols ? 2 : 1);
 }
 
+// Work of one CTA as a list of pieces: a piece is K blocks [kb0, kb1) of unit
+// u, the pi-th of the np pieces that unit is cut into.
+//  mode 0: every unit cut into S equal K ranges (S = 1: whole units); CTA c
+//          takes pieces c, c + grid, c + 2 grid, ... of the unit-major list.
+//  mode 1 (stream-K): the units' K blocks laid end to end, CTA c takes blocks
+//          [c*total/grid, (c+1)*total/grid); a unit cut between CTAs becomes
+//          several pieces.
+// A unit of np > 1 pieces is finished by whichever piece arrives last.
+struct Piece {
+  int u, kb0, kb1, pi, np;
+};
+
+struct WorkIter {
+  int mode, S, units, kblocks, grid, cta;
+  long long cur, end, total;
+  __device__ static long long start_of(int c, long long total, int grid) {
+    return static_cast<long long>(c) * total / grid;
+  }
+  __device__ int cta_of(long long kk) const {   // CTA whose range holds K block kk
+    int c = static_cast<int>(kk * grid / total);
+    while (c + 1 < grid && start_of(c + 1, total, grid) <= kk) ++c;
+    while (c > 0 && start_of(c, total, grid) > kk) --c;
+    return c;
+  }
+  __device__ WorkIter(int mode_, int S_, int units_, int kblocks_, int grid_, int cta_)
+      : mode(mode_), S(S_), units(units_), kblocks(kblocks_), grid(grid_), cta(cta_) {
+    total = static_cast<long long>(units) * kblocks;
+    if (mode == 0) {
+      cur = cta;
+      end = static_cast<long long>(units) * S;
+    } else {
+      cur = start_of(cta, total, grid);
+      end = start_of(cta + 1, total, grid);
+    }
+  }
+  __device__ bool empty() const { return cur >= end; }
+  __device__ bool next(Piece& p) {
+    if (cur >= end) return false;
+    if (mode == 0) {
+      const int u = static_cast<int>(cur / S), sp = static_cast<int>(cur - static_cast<long long>(u) * S);
+      const int per = kblocks / S;
+      p = Piece{u, sp * per, (sp + 1) * per, sp, S};
+      cur += grid;
+      return true;
+    }
+    const int u = static_cast<int>(cur / kblocks);
+    const int kb0 = static_cast<int>(cur - static_cast<long long>(u) * kblocks);
+    const long long left = end - cur;
+    const int kb1 = left < kblocks - kb0 ? kb0 + static_cast<int>(left) : kblocks;
+    const int first = cta_of(static_cast<long long>(u) * kblocks);
+    const int last = cta_of(static_cast<long long>(u) * kblocks + kblocks - 1);
+    p = Piece{u, kb0, kb1, cta - first, last - first + 1};
+    cur += kb1 - kb0;
+    return true;
+  }
+};
+
+// Cost of a piece beyond its K blocks (epilogue, partial store, ticket, the
+// last arriver's sum), in K blocks; measured on decode shapes.
+constexpr int kPieceCost = 6;
+
 template <int SWAP, int W, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_wgt,
@@ -120,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
-  int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] split S, [1] last arriver, [2..5] warp ok
+  int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] mode, [1] last arriver, [2..5] warp ok, [6] P, [7] S
   int* s_off = reinterpret_cast<int*>(smem + C::kStages * C::kStageBytes + 256);   // [G+1]
   int* s_ustart = s_off + (kMaxGroups + 1);                                          // [G+1]
 
@@ -178,30 +239,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool any_bad = __any_sync(0xffffffffu, bad);
     const int units = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) {
-      int S = 1;
-      if (SWAP && args.counters && mx <= kSplitRows && units <= args.unit_cap) {
-        // sub-units per CTA x (K blocks per sub-unit + a fixed cost of 2 blocks)
-        const int grid = static_cast<int>(gridDim.x);
-        long long best = static_cast<long long>((units + grid - 1) / grid) * (kblocks + 2);
+      // the cheapest of: S-way splits (S = 1, 2, 4, 8) and stream-K, costed as
+      // the longest CTA's K blocks plus kPieceCost per piece it runs;
+      // P = the most pieces one unit can be cut into
+      int mode = 0, S = 1, P = 1;
+      const int grid = static_cast<int>(gridDim.x);
+      if (SWAP && args.counters && mx <= kSplitRows && units > 0 && units <= args.unit_cap) {
+        long long best = static_cast<long long>((units + grid - 1) / grid) * (kblocks + kPieceCost);
         for (int c = 2; c <= kMaxSplit; c *= 2) {
           if (kblocks % c || static_cast<long long>(units) * c > args.split_cap) continue;
-          const long long cost = ((static_cast<long long>(units) * c + grid - 1) / grid) * (kblocks / c + 2);
-          if (cost < best) { best = cost; S = c; }
+          const long long cost =
+              ((static_cast<long long>(units) * c + grid - 1) / grid) * (kblocks / c + kPieceCost);
+          if (cost < best) { best = cost; S = c; P = c; }
+        }
+        const long long tot = static_cast<long long>(units) * kblocks;
+        const long long share = tot / grid;
+        if (share >= 1) {
+          const int psk = static_cast<int>((kblocks + share - 1) / share) + 1;
+          const long long pieces_per_cta = (share + kblocks - 1) / kblocks + 1;
+          const long long cost = (tot + grid - 1) / grid + kPieceCost * pieces_per_cta;
+          if (cost < best && static_cast<long long>(units) * psk <= args.split_cap) {
+            best = cost; mode = 1; S = 1; P = psk;
+          }
         }
       }
-      s_split[0] = S;
-      *s_total = any_bad ? 0 : units * S;
+      s_split[0] = mode;
+      s_split[6] = P;
+      s_split[7] = S;
+      *s_total = any_bad ? 0 : units;
       *abort_flag = 0;
       if (any_bad && blockIdx.x == 0) set_status(args.status, MOE_ERR_DEVICE_CHECK);
     }
   }
   __syncthreads();
-  const int total = *s_total;
-  const int S = s_split[0];
-  const int kb_per = kblocks / S;
-  // a CTA without units (or every CTA, when the offsets failed their check)
+  const int units = *s_total;
+  const int mode = s_split[0];
+  const int P = s_split[6];
+  const int S = s_split[7];
+  // a CTA without work (or every CTA, when the offsets failed their check)
   // leaves before it allocates tensor memory
-  if (static_cast<int>(blockIdx.x) >= total) return;
+  if (units == 0 || WorkIter(mode, S, units, kblocks, gridDim.x, blockIdx.x).empty()) return;
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
@@ -238,16 +315,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long issued = 0;
       int stage = 0;
       uint32_t phase = 0;
-      for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
-        const int u = idx / S, sp = idx - u * S;
+      WorkIter wi(mode, S, units, kblocks, gridDim.x, blockIdx.x);
+      Piece pc;
+      while (wi.next(pc)) {
         int g, row0, nrows, wb;
-        decode(u, g, row0, nrows, wb);
+        decode(pc.u, g, row0, nrows, wb);
         const int wrow = g * wrows + wb * C::kOutCols;
         const int n16 = (nrows + 15) >> 4;
         const uint32_t bytes = SWAP ? static_cast<uint32_t>(C::kABytes + n16 * 16 * kBK * 2)
                                     : static_cast<uint32_t>(C::kStageBytes);
         bool ok = true;
-        for (int kb = sp * kb_per; kb < (sp + 1) * kb_per; ++kb) {
+        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status)) { ok = false; break; }
           uint8_t* sa = stage_base + stage * C::kStageBytes;
           uint8_t* sb = sa + C::kABytes;
@@ -286,15 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int idx = blockIdx.x; idx < total; idx += gridDim.x, ++it) {
+      WorkIter wi(mode, S, units, kblocks, gridDim.x, blockIdx.x);
+      Piece pc;
+      for (; wi.next(pc); ++it) {
         const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
         const uint32_t aphase = (C::kNumAcc == 2 ? (it >> 1) : it) & 1;
-        const int u = idx / S, sp = idx - u * S;
         uint32_t idesc;
         int chains = 1, cw = 0;
         if (SWAP) {
           int g, row0, nrows, wb;
-          decode(u, g, row0, nrows, wb);
+          decode(pc.u, g, row0, nrows, wb);
           const int n16 = (nrows + 15) >> 4;
           idesc = idesc_bf16_f32(128, n16 * 16);
           chains = swap_chains(n16, C::kAccCols, ACT == 1);
@@ -305,9 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&tempty_bar[ab], aphase ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * C::kAccCols;
-        const int kb0 = sp * kb_per;
+        const int kb0 = pc.kb0;
         bool ok = true;
-        for (int kb = kb0; kb < kb0 + kb_per; ++kb) {
+        for (int kb = kb0; kb < pc.kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * C::kStageBytes);
@@ -345,14 +424,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                    // TMEM lane quadrant of this warp
     const int lrow = q * 32 + lane;            // TMEM lane = accumulator row
     int it = 0;
-    for (int idx = blockIdx.x; idx < total; idx += gridDim.x, ++it) {
+    WorkIter wi(mode, S, units, kblocks, gridDim.x, blockIdx.x);
+    Piece pc;
+    for (; wi.next(pc); ++it) {
       const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
       const uint32_t aphase = (C::kNumAcc == 2 ? (it >> 1) : it) & 1;
-      const int u = idx / S, sp = idx - u * S;
+      const int u = pc.u;
       int g, row0, nrows, wb;
       decode(u, g, row0, nrows, wb);
       bool ok = mbar_wait(&tfull_bar[ab], aphase, abort_flag, args.status);
-      if (S > 1) {
+      if (P > 1) {
         // the split path meets at named barriers: the four warps leave together or not at all
         if (lane == 0) s_split[2 + q] = ok ? 1 : 0;
         epi_bar_sync();
@@ -394,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         };
-        if (S == 1) {
+        if (pc.np == 1) {
 #pragma unroll 1
           for (int j = 0; j < n16; ++j) {
             float gs[16], us[16];
@@ -409,26 +490,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           release_acc();
         } else {
-          // split-K: nrows <= 16, one 16-token chunk holds the whole partial
+          // a piece of a unit cut between CTAs (nrows <= 16: one 16-token
+          // chunk holds the whole partial)
           constexpr int PF = partial_floats<ACT>();
           float gm[16], um[16];
           load_chunk(0, gm, um);
           release_acc();
-          float4* mine = reinterpret_cast<float4*>(args.partials + (static_cast<size_t>(idx) * 128 + lrow) * PF);
+          float4* mine = reinterpret_cast<float4*>(
+              args.partials + ((static_cast<size_t>(u) * P + pc.pi) * 128 + lrow) * PF);
+          const int n4 = (nrows + 3) >> 2;   // float4s per half that hold live tokens
 #pragma unroll
           for (int i = 0; i < kSplitRows / 4; ++i) {
-            mine[i] = make_float4(gm[4 * i], gm[4 * i + 1], gm[4 * i + 2], gm[4 * i + 3]);
-            if (ACT == 1) mine[kSplitRows / 4 + i] = make_float4(um[4 * i], um[4 * i + 1], um[4 * i + 2], um[4 * i + 3]);
+            if (i < n4) {
+              mine[i] = make_float4(gm[4 * i], gm[4 * i + 1], gm[4 * i + 2], gm[4 * i + 3]);
+              if (ACT == 1) mine[kSplitRows / 4 + i] = make_float4(um[4 * i], um[4 * i + 1], um[4 * i + 2], um[4 * i + 3]);
+            }
           }
           __threadfence();
           epi_bar_sync();
           if (threadIdx.x == 64) {
             const int old = atomicAdd(&args.counters[u], 1);
             int last = 0;
-            if (old == S - 1) {
+            if (old == pc.np - 1) {
               last = 1;
               atomicExch(&args.counters[u], 0);   // every ticket of this unit is taken: back to zero
-            } else if (old < 0 || old >= S) {
+            } else if (old < 0 || old >= pc.np) {
               set_status(args.status, MOE_ERR_DEVICE_CHECK);   // counters were not zero at entry
             }
             s_split[1] = last;
@@ -439,22 +525,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             float gs[kSplitRows], us[kSplitRows];
 #pragma unroll
             for (int i = 0; i < kSplitRows; ++i) { gs[i] = 0.f; us[i] = 0.f; }
-            for (int j = 0; j < S; ++j) {   // split order, whoever arrived last
-              if (j == sp) {
+            const float4* slot0 = reinterpret_cast<const float4*>(
+                args.partials + (static_cast<size_t>(u) * P * 128 + lrow) * PF);
+            const size_t slot_f4 = static_cast<size_t>(128) * PF / 4;   // float4s per piece slot
 #pragma unroll
-                for (int i = 0; i < kSplitRows; ++i) { gs[i] += gm[i]; us[i] += um[i]; }
-              } else {
-                const float4* src = reinterpret_cast<const float4*>(
-                    args.partials + (static_cast<size_t>(u * S + j) * 128 + lrow) * PF);
-#pragma unroll
-                for (int i = 0; i < kSplitRows / 4; ++i) {
-                  const float4 v = __ldcg(src + i);
-                  gs[4 * i] += v.x; gs[4 * i + 1] += v.y; gs[4 * i + 2] += v.z; gs[4 * i + 3] += v.w;
-                  if (ACT == 1) {
-                    const float4 w4 = __ldcg(src + kSplitRows / 4 + i);
-                    us[4 * i] += w4.x; us[4 * i + 1] += w4.y; us[4 * i + 2] += w4.z; us[4 * i + 3] += w4.w;
-                  }
+            for (int i = 0; i < kSplitRows / 4; ++i) {
+              if (i >= n4) break;
+              // pieces in order, whoever arrived last; the loads of all pieces
+              // are independent and go out together
+#pragma unroll 8
+              for (int j = 0; j < pc.np; ++j) {
+                float4 a, b;
+                if (j == pc.pi) {
+                  a = make_float4(gm[4 * i], gm[4 * i + 1], gm[4 * i + 2], gm[4 * i + 3]);
+                  b = make_float4(um[4 * i], um[4 * i + 1], um[4 * i + 2], um[4 * i + 3]);
+                } else {
+                  a = __ldcg(slot0 + j * slot_f4 + i);
+                  b = ACT == 1 ? __ldcg(slot0 + j * slot_f4 + kSplitRows / 4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+                gs[4 * i] += a.x; gs[4 * i + 1] += a.y; gs[4 * i + 2] += a.z; gs[4 * i + 3] += a.w;
+                us[4 * i] += b.x; us[4 * i + 1] += b.y; us[4 * i + 2] += b.z; us[4 * i + 3] += b.w;
               }
             }
 #pragma unroll
