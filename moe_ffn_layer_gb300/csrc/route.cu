@@ -25,8 +25,9 @@
 //             bf16(w - hi - mid); every subtraction is exact in fp32 and the
 //             three terms carry the full 24-bit significand), and since x is
 //             bf16 every product x*term is exact in fp32; the grouped GEMM
-//             adds them in fp32 with K = 3H.  Other sizes: router_tile, an fp32
-//             SIMT tile GEMM, 64 tokens x 64 experts per CTA.
+//             adds them in fp32 with K = 3H.  Fewer tokens: fp32 FMAs, one
+//             warp per (expert, 16 tokens) below 512 tokens, else a 64 x 64
+//             SIMT tile GEMM.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -98,6 +99,53 @@ __global__ void __launch_bounds__(256)
       const int e = e0 + tx * 4 + j;
       if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j];
     }
+  }
+}
+
+// 16 < T < 512: one warp per (expert, chunk of 16 tokens); lanes stride H
+// eight elements at a time (16-byte loads, all independent), each lane keeps
+// 16 fp32 partial sums, then a fixed butterfly adds the lanes.  Wr rows are
+// read once per chunk (from L2 after the first).
+constexpr int kChunkT = 16;
+
+__global__ void __launch_bounds__(256)
+    router_gemv_chunk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, int T, int H, int E,
+                             float* __restrict__ logits) {
+  chain_wait();
+  const ChainReleaseAtExit release_next;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int e = gw % E, t0 = (gw / E) * kChunkT;
+  if (t0 >= T) return;
+  const int nt = min(kChunkT, T - t0);
+  float acc[kChunkT];
+#pragma unroll
+  for (int t = 0; t < kChunkT; ++t) acc[t] = 0.f;
+  const float* w = wr + static_cast<size_t>(e) * H;
+  const __nv_bfloat16* xc = x + static_cast<size_t>(t0) * H;
+#pragma unroll 2
+  for (int h0 = lane * 8; h0 < H; h0 += 256) {
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + h0));
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + h0 + 4));
+#pragma unroll
+    for (int t = 0; t < kChunkT; ++t) {
+      if (t < nt) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xc + static_cast<size_t>(t) * H + h0));
+        float f[8];
+        bf16x8_to_f32(xv, f);
+        float v = acc[t];
+        v = fmaf(f[0], w0.x, v); v = fmaf(f[1], w0.y, v); v = fmaf(f[2], w0.z, v); v = fmaf(f[3], w0.w, v);
+        v = fmaf(f[4], w1.x, v); v = fmaf(f[5], w1.y, v); v = fmaf(f[6], w1.z, v); v = fmaf(f[7], w1.w, v);
+        acc[t] = v;
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kChunkT; ++t) {
+    float v = acc[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == t && t < nt) logits[static_cast<size_t>(t0 + t) * E + e] = v;
   }
 }
 
@@ -440,6 +488,12 @@ int route_launch(const void* x, const float* w_router, const float* bias, int T,
     ++*launches;
     const int rc = router_gemm_launch(x, wr3, T, H, E, logits_ws, status, grid_cap, stream, launches);
     if (rc) return rc;
+  } else if (T < kTcMinT) {
+    const long long warps = static_cast<long long>(E) * ((T + kChunkT - 1) / kChunkT);
+    if (launch_chained(router_gemv_chunk_kernel, dim3(static_cast<int>((warps + 7) / 8)), dim3(256), 0, stream, xb,
+                       w_router, T, H, E, logits_ws) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    ++*launches;
   } else {
     dim3 grid((T + kRT - 1) / kRT, (E + kRE - 1) / kRE);
     if (launch_chained(router_tile_kernel, grid, dim3(256), 0, stream, xb, w_router, T, H, E, logits_ws) != cudaSuccess)
