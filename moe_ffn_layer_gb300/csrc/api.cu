@@ -81,7 +81,8 @@ Layout layout(const moe_dims* d, int T) {
   L.sorted = take(Tk * 4);
   L.inv = take(Tk * 4);
   L.pcounts = take(moe::permute_ws_bytes(T, d->E));
-  L.xperm = take(Tk * d->H * 2);
+  // decode sizes gather the dispatched rows inside gmm1; larger batches copy them
+  L.xperm = take(T <= moe::route_small_max_tokens() ? 0 : Tk * d->H * 2);
   L.h = take(Tk * d->I * 2);
   L.y = take(Tk * d->H * 2);
   L.hs = take(static_cast<size_t>(T) * d->I_s * 2);
@@ -245,11 +246,11 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
   int32_t* sorted = reinterpret_cast<int32_t*>(base + L.sorted);
   int32_t* inv = reinterpret_cast<int32_t*>(base + L.inv);
   int32_t* pcounts = reinterpret_cast<int32_t*>(base + L.pcounts);
-  void* xperm = base + L.xperm;
   void* h = base + L.h;
   void* y = base + L.y;
   void* hs = base + L.hs;
   void* s = base + L.s;
+  void* xperm = base + L.xperm;
   void* gmain = base + L.gemm_main;
   void* gside = base + L.gemm_side;
   const int rows = T * d->k;
@@ -269,8 +270,8 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
   }
   // routed path on `stream`: route -> dispatch -> gmm1 (+SiLU*mul) -> gmm2
   if (T <= moe::route_small_max_tokens()) {
-    // decode sizes: router, top-k, counting sort and row gather in one launch
-    const moe::DispatchOut dout{offsets, sorted, inv, xperm};
+    // decode sizes: router, top-k and counting sort in one launch
+    const moe::DispatchOut dout{offsets, sorted, inv, nullptr};
     rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, &dout, di->status,
                            di->sms, stream, &n);
   } else {
@@ -281,8 +282,15 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
                                di->sms, stream, &n);
   }
   if (!rc)
-    rc = moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, gmain,
-                                  L.gemm_main_bytes, di->sms, stream, &n);
+    // decode sizes: gmm1 reads the dispatched rows straight from x through
+    // sorted_token (TMA gather4, a few rows per stage); larger batches read the
+    // permuted copy, since one producer thread issuing a gather per 4 rows
+    // cannot feed full 128-row tiles
+    rc = T <= moe::route_small_max_tokens()
+             ? moe::grouped_gemm_launch(x, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, gmain,
+                                        L.gemm_main_bytes, di->sms, stream, &n, sorted, T)
+             : moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status,
+                                        gmain, L.gemm_main_bytes, di->sms, stream, &n);
   if (!rc)
     rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, gmain,
                                   L.gemm_main_bytes, di->sms, stream, &n);

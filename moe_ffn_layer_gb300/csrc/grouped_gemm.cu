@@ -64,12 +64,13 @@ struct Cfg {
   static constexpr int kAccCols = SWAP ? (ACT == 1 ? 2 : 1) * W : W;             // TMEM columns per unit
   static constexpr int kNumAcc = 2 * kAccCols <= 512 ? 2 : 1;
   static constexpr int kTmemCols = tmem_cols_pow2(kNumAcc * kAccCols);
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256 + 2 * (kMaxGroups + 1) * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256 + 2 * (kMaxGroups + 1) * 4 + 128 * 4;
   static_assert(kStages >= 2, "ring too shallow");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 constexpr int kSplitRows = 16;     // split-K only when every group has <= 16 rows
+constexpr int kBM_rows = 128;      // token rows of a tokens-on-M unit
 constexpr int kMaxSplit = 8;
 
 struct GemmArgs {
@@ -87,6 +88,8 @@ struct GemmArgs {
   int unit_cap;            // units the counters cover
   int a_kblocks;           // > 0: A has this many K blocks and is re-read for every
                            // run of them along B's K (tokens-on-M form only)
+  const int32_t* a_rows;   // non-null: token row r is row a_rows[r] of the token tensor
+                           // (fetched with TMA gather4; no permuted copy needed)
 };
 
 // fp32 values one TMEM lane keeps per split-K partial
@@ -184,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] mode, [1] last arriver, [2..5] warp ok, [6] P, [7] S
   int* s_off = reinterpret_cast<int*>(smem + C::kStages * C::kStageBytes + 256);   // [G+1]
   int* s_ustart = s_off + (kMaxGroups + 1);                                          // [G+1]
+  int* s_gidx = s_ustart + (kMaxGroups + 1);                                         // [128] gathered rows
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -309,36 +313,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_tok = l2_policy_evict_last();
-      const uint64_t pol_w = args.stream_w ? l2_policy_evict_first() : l2_policy_evict_normal();
-      long long issued = 0;
-      int stage = 0;
-      uint32_t phase = 0;
-      WorkIter wi(mode, S, units, kblocks, gridDim.x, blockIdx.x);
-      Piece pc;
-      while (wi.next(pc)) {
-        int g, row0, nrows, wb;
-        decode(pc.u, g, row0, nrows, wb);
-        const int wrow = g * wrows + wb * C::kOutCols;
-        const int n16 = (nrows + 15) >> 4;
-        const uint32_t bytes = SWAP ? static_cast<uint32_t>(C::kABytes + n16 * 16 * kBK * 2)
-                                    : static_cast<uint32_t>(C::kStageBytes);
-        bool ok = true;
+    // lane 0 issues the copies; with gathered rows the whole warp first
+    // stages the unit's source row indices in shared memory
+    const uint64_t pol_tok = l2_policy_evict_last();
+    const uint64_t pol_w = args.stream_w ? l2_policy_evict_first() : l2_policy_evict_normal();
+    long long issued = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    WorkIter wi(mode, S, units, kblocks, gridDim.x, blockIdx.x);
+    Piece pc;
+    while (wi.next(pc)) {
+      int g, row0, nrows, wb;
+      decode(pc.u, g, row0, nrows, wb);
+      const int wrow = g * wrows + wb * C::kOutCols;
+      const int n16 = (nrows + 15) >> 4;
+      // token rows fetched: SWAP 16-row multiples; tokens-on-M all 128 rows
+      // (whole box) or, gathered, the live rows rounded up to 4
+      const int nfetch = SWAP ? n16 * 16 : (args.a_rows ? (nrows + 3) & ~3 : kBM_rows);
+      if (args.a_rows) {
+        __syncwarp();
+        for (int i = lane; i < nfetch; i += 32) s_gidx[i] = args.a_rows[row0 + min(i, nrows - 1)];
+        __syncwarp();
+      }
+      const uint32_t bytes = static_cast<uint32_t>(C::kABytes * (SWAP ? 1 : 0) + C::kBBytes * (SWAP ? 0 : 1) +
+                                                   nfetch * kBK * 2);
+      bool ok = true;
+      if (lane == 0) {
         for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status)) { ok = false; break; }
           uint8_t* sa = stage_base + stage * C::kStageBytes;
           uint8_t* sb = sa + C::kABytes;
           const int kc = kb * kBK;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          uint8_t* stok = SWAP ? sb : sa;   // where the token rows go
           if (SWAP) {
             tma_load_2d(sa, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
             if (ACT == 1) tma_load_2d(sa + kTileRows128, &tm_wgt, &full_bar[stage], kc, wrow + args.N, pol_w);
-            for (int j = 0; j < n16; ++j)
-              tma_load_2d(sb + j * 16 * kBK * 2, &tm_tok, &full_bar[stage], kc, row0 + 16 * j, pol_tok);
           } else {
-            const int kca = args.a_kblocks ? (kb % args.a_kblocks) * kBK : kc;
-            tma_load_2d(sa, &tm_tok, &full_bar[stage], kca, row0, pol_tok);
             if (ACT == 1) {
               tma_load_2d(sb, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
               tma_load_2d(sb + (W / 2) * kBK * 2, &tm_wgt, &full_bar[stage], kc, wrow + args.N, pol_w);
@@ -346,11 +357,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sb, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
             }
           }
+          if (args.a_rows) {
+            for (int j = 0; j < nfetch; j += 4)
+              tma_gather4(stok + j * kBK * 2, &tm_tok, &full_bar[stage], kc, s_gidx[j], s_gidx[j + 1],
+                          s_gidx[j + 2], s_gidx[j + 3], pol_tok);
+          } else if (SWAP) {
+            for (int j = 0; j < n16; ++j)
+              tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &full_bar[stage], kc, row0 + 16 * j, pol_tok);
+          } else {
+            const int kca = args.a_kblocks ? (kb % args.a_kblocks) * kBK : kc;
+            tma_load_2d(stok, &tm_tok, &full_bar[stage], kca, row0, pol_tok);
+          }
           ++issued;
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
       }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    }
+    if (lane == 0) {
       // drain: every load issued into the ring has landed before the CTA may
       // exit (bounded wait that ignores `abort`; the normal path passes at once)
       for (int s = 0; s < C::kStages; ++s) {
@@ -688,7 +712,7 @@ SplitPlan split_plan(int G, int rows_max, int N, int act, int max_slots = kMaxSl
 template <int SWAP, int W, int ACT>
 int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K, void* out,
                int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream, int* launches,
-               int max_slots = kMaxSlots, int K_a = 0) {
+               int max_slots = kMaxSlots, int K_a = 0, const int32_t* a_rows = nullptr, int a_src_rows = 0) {
   using C = Cfg<SWAP, W, ACT>;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -703,15 +727,18 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   const int wrows = ACT == 1 ? 2 * N : N;
   const uint32_t tok_box = SWAP ? 16 : 128;
   const uint32_t wgt_box = SWAP ? 128 : (ACT == 1 ? W / 2 : W);
-  if (!make_map(&tt, a, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K_a ? K_a : K), tok_box))
+  if (a_rows) {   // rows fetched one at a time by gather4: a one-row box over the source rows
+    if (!make_map(&tt, a, static_cast<uint64_t>(a_src_rows), static_cast<uint64_t>(K), 1)) return MOE_ERR_CUDA;
+  } else if (!make_map(&tt, a, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K_a ? K_a : K), tok_box)) {
     return MOE_ERR_CUDA;
+  }
   if (!make_map(&tw, w, static_cast<uint64_t>(G) * wrows, static_cast<uint64_t>(K), wgt_box)) return MOE_ERR_CUDA;
   // upper bound on the unit count: every non-empty group adds at most one partial row block
   const long long nonempty = offsets ? (G < rows_max ? G : rows_max) : 1;
   long long bound =
       (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) * (N / C::kOutCols);
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
-                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0};
+                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows};
   if (SWAP && ws) {
     const SplitPlan p = split_plan(G, rows_max, N, ACT, max_slots);
     if (p.bytes && ws_bytes >= p.bytes) {
@@ -743,29 +770,30 @@ size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act) {
 
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream,
-                        int* launches) {
+                        int* launches, const int32_t* a_rows, int a_src_rows) {
   if (rows_max == 0) return MOE_OK;
   if (grouped_gemm_weights_on_m(G, rows_max, N)) {
     if (act == 1)
       return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap,
-                                         stream, launches);
+                                         stream, launches, kMaxSlots, 0, a_rows, a_src_rows);
     return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap, stream,
-                                       launches);
+                                       launches, kMaxSlots, 0, a_rows, a_src_rows);
   }
   if (act == 1) {
     if (N % 128 == 0)
       return launch_cfg<0, 256, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
-                                   launches);
+                                   launches, kMaxSlots, 0, a_rows, a_src_rows);
     return launch_cfg<0, 128, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
-                                 launches);
+                                 launches, kMaxSlots, 0, a_rows, a_src_rows);
   }
   if (N % 256 == 0)
     return launch_cfg<0, 256, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
-                                 launches);
+                                 launches, kMaxSlots, 0, a_rows, a_src_rows);
   if (N % 128 == 0)
     return launch_cfg<0, 128, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
-                                 launches);
-  return launch_cfg<0, 64, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream, launches);
+                                 launches, kMaxSlots, 0, a_rows, a_src_rows);
+  return launch_cfg<0, 64, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream, launches,
+                              kMaxSlots, 0, a_rows, a_src_rows);
 }
 
 size_t grouped_gemm_counter_bytes(int G, int rows_max, int N, int act) {

@@ -33,9 +33,11 @@ bool grouped_gemm_weights_on_m(int G, int rows_max, int N);
 // Split-K scratch bytes of a launch (0: never splits).
 size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act);
 // ws (nullable): split-K scratch, zero-filled before its first use; left zero.
+// a_rows (nullable): token row r of the product is row a_rows[r] of `a`, a
+// [a_src_rows][K] tensor (rows fetched by TMA gather4, no permuted copy).
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream,
-                        int* launches);
+                        int* launches, const int32_t* a_rows = nullptr, int a_src_rows = 0);
 // Bytes at the start of the split-K scratch that hold the ticket counters.
 size_t grouped_gemm_counter_bytes(int G, int rows_max, int N, int act);
 // The same with at most max_slots split-K partial slots (a smaller scratch).

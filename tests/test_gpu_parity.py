@@ -351,6 +351,20 @@ def test_forward_one_hot_expert_and_empty_experts():
     assert_close_layer(to_f64(out), ref["out"], "hot expert")
 
 
+@pytest.mark.parametrize("T,I", [(12, 64), (16, 192), (3, 128)])
+def test_forward_decode_gathered_rows(T, I):
+    """At decode sizes the first matmul reads the dispatched rows of x through
+    sorted_token (TMA gather4) in both tile forms: I a multiple of 128 gives the
+    weights-on-M form, otherwise tokens-on-M."""
+    wl = synth.Workload("gather", T, 128, 8, 2, I, 64, sigma_router=0.2, sigma_w=0.05)
+    inp = synth.make_inputs(wl, 13)
+    ref = om.forward(inp, wl.k)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    out = L.forward(bf16_tensor(inp["x"], "cuda"))
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], f"gathered rows T={T} I={I}")
+
+
 def test_forward_without_shared_expert():
     wl = synth.Workload("noshared", 40, 128, 8, 2, 64, 0, sigma_router=0.1)
     inp = synth.make_inputs(wl, 12)
