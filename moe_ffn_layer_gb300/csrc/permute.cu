@@ -1,7 +1,7 @@
 // Dispatch of the MoE FFN layer at one expert-parallel rank: a counting sort of
 // the T*k (token, slot) pairs by (expert ascending, token ascending), the
 // per-expert row offsets of the grouped matmuls, the inverse map used by the
-// combine, and the row gather x_perm[r] = x[sorted_token[r]].
+// combine, and the row copy x_perm[r] = x[sorted_token[r]].
 //
 // "dispatch" is the step before gmm1 on the routed path ("Ascend 910C LLM
 // inference optimisation, part 2" (Dewu Tech), section on MoE multi-stream
@@ -218,22 +218,30 @@ __global__ void __launch_bounds__(kTB)
   }
 }
 
-// x_perm[r] = x[sorted_token[r]] for r < offsets[E]; one warp per row, 16-byte
-// loads and stores.
+// x_perm[inv_perm[t*k + j]] = x[t]: one warp per token reads its row once (16-byte
+// loads) and writes its k copies, so x is read from memory once even when it
+// does not fit in L2.  Pairs the sort rejected (row -1) are skipped.
 __global__ void __launch_bounds__(256)
-    gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_token,
-                       const int32_t* __restrict__ offsets, int E, int T, int H, uint4* __restrict__ x_perm) {
+    scatter_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_perm, int T, int H, int k,
+                        long long rows_max, uint4* __restrict__ x_perm) {
   chain_wait();
   const ChainReleaseAtExit release_next;
-  const int rows = offsets[E];
   const int vec = H / 8;
   const int lane = threadIdx.x & 31;
-  for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += gridDim.x * 8) {
-    const int t = sorted_token[r];
-    if (t < 0 || t >= T) continue;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+    int dst[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      const int r = j < k ? inv_perm[static_cast<size_t>(t) * k + j] : -1;
+      dst[j] = (r >= 0 && r < rows_max) ? r : -1;
+    }
     const uint4* src = x + static_cast<size_t>(t) * vec;
-    uint4* dst = x_perm + static_cast<size_t>(r) * vec;
-    for (int i = lane; i < vec; i += 32) dst[i] = src[i];
+    for (int i = lane; i < vec; i += 32) {
+      const uint4 v = __ldg(src + i);
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (dst[j] >= 0) x_perm[static_cast<size_t>(dst[j]) * vec + i] = v;
+    }
   }
 }
 
@@ -265,12 +273,11 @@ int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, 
     *launches += 3;
   }
   if (x_perm) {
-    const long long rows = static_cast<long long>(T) * k;
-    long long grid = (rows + 7) / 8;
+    long long grid = (static_cast<long long>(T) + 7) / 8;
     if (grid > 8LL * num_sms) grid = 8LL * num_sms;
-    if (launch_chained(gather_rows_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, stream,
-                       static_cast<const uint4*>(x), static_cast<const int32_t*>(sorted_token),
-                       static_cast<const int32_t*>(offsets), E, T, H, static_cast<uint4*>(x_perm)) != cudaSuccess)
+    if (launch_chained(scatter_rows_kernel, dim3(static_cast<int>(grid)), dim3(256), 0, stream,
+                       static_cast<const uint4*>(x), static_cast<const int32_t*>(inv_perm), T, H, k,
+                       static_cast<long long>(T) * k, static_cast<uint4*>(x_perm)) != cudaSuccess)
       return MOE_ERR_CUDA;
     ++*launches;
   }
