@@ -131,8 +131,10 @@ MOE_API int moe_permute(const int32_t* topk_ids, const void* x, int T, int H, in
  *  ws            split-K scratch of moe_grouped_gemm_workspace_bytes(...) bytes,
  *                256-byte aligned, or NULL (no split-K).  It must be zero-filled
  *                before its first use; every call leaves its counters zero
- *                again (after a device error, zero it again).  Calls that share
- *                a scratch buffer must not overlap on the GPU.
+ *                again (after a device error, zero it again).  The counters
+ *                fill the first 64 KiB whatever the shape, so calls of any
+ *                shapes may use one buffer in turn (sized for the largest).
+ *                Calls that share a scratch buffer must not overlap on the GPU.
  * bf16 inputs, fp32 accumulation in tensor memory, bf16 (round-to-nearest)
  * output.  With scratch, launches whose groups have at most 16 rows may cut a
  * unit's K range between CTAs (S-way split or stream-K); the partial sums are
@@ -158,7 +160,9 @@ MOE_API int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_
  *  - Every call uses the same array and it keeps the previous call's data:
  *    calls that overlap on the GPU (other streams, other threads) race on it
  *    and give wrong results.  Order them on one stream.
- *  - A problem whose scratch would exceed the array returns MOE_ERR_WORKSPACE. */
+ *  - A launch uses at most a 64 KiB counter region plus 1024 partial slots of
+ *    at most 16 KiB, so every supported shape fits the array (the call checks
+ *    this and would return MOE_ERR_WORKSPACE). */
 #define MOE_NOALLOC_SCRATCH_BYTES (24u << 20)
 MOE_API int moe_grouped_gemm_noalloc(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max,
                                      int N, int K, int act, void* out, cudaStream_t stream);
@@ -178,8 +182,10 @@ MOE_API int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const 
  * `side` and the events may be NULL when d->I_s == 0.  ws holds every
  * intermediate and the split-K scratch of the four matmuls; size it with
  * moe_workspace_bytes(d, T), align it to 256 bytes and zero-fill it before its
- * first use (calls leave the scratch counters zero).  Calls that share a
- * workspace must not overlap on the GPU.
+ * first use (calls leave the scratch counters zero).  The counters sit at the
+ * same offsets for every T, so calls with different T may use one workspace
+ * sized for the largest.  Calls that share a workspace must not overlap on
+ * the GPU.
  *  x bf16 [T][H] (device);  out bf16 [T][H] (device) */
 MOE_API size_t moe_workspace_bytes(const moe_dims* d, int T);
 MOE_API int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, void* out, void* ws,

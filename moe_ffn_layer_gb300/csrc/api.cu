@@ -55,10 +55,13 @@ int dev_info(DevInfo** out) {
   return MOE_OK;
 }
 
+constexpr size_t kRouteTicketBytes = 256;   // moe_route's ws: [ticket | logits scratch]
+
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Every intermediate of moe_forward, 256-byte aligned, in one caller-owned buffer.
 struct Layout {
+  size_t ctr_main, ctr_side, route_ticket;   // counters: first, at offsets that do not depend on T
   size_t gemm_main, gemm_main_bytes, gemm_side, gemm_side_bytes;
   size_t logits, ids, w, offsets, sorted, inv, pcounts, xperm, h, y, hs, s, total;
 };
@@ -72,14 +75,20 @@ Layout layout(const moe_dims* d, int T) {
     return r;
   };
   const size_t Tk = static_cast<size_t>(T) * d->k;
-  // split-K scratch: one region for the routed pair (main stream), one for the
-  // shared pair (side stream), so the two streams never share counters
+  // split-K scratch: one set for the routed pair (main stream), one for the
+  // shared pair (side stream), so the two streams never share counters.  The
+  // counters come first, at the same offsets for every T, so that calls with
+  // different T can share one workspace in turn: the region that holds one
+  // call's counters never holds another call's data.
   const int rows = T * d->k;
-  L.gemm_main_bytes = std::max(moe::grouped_gemm_ws_bytes(d->E, rows, d->I, 1),
-                               moe::grouped_gemm_ws_bytes(d->E, rows, d->H, 0));
-  L.gemm_side_bytes = d->I_s ? std::max(moe::grouped_gemm_ws_bytes(1, T, d->I_s, 1),
-                                        moe::grouped_gemm_ws_bytes(1, T, d->H, 0))
+  L.gemm_main_bytes = std::max(moe::grouped_gemm_partial_bytes(d->E, rows, d->I, 1),
+                               moe::grouped_gemm_partial_bytes(d->E, rows, d->H, 0));
+  L.gemm_side_bytes = d->I_s ? std::max(moe::grouped_gemm_partial_bytes(1, T, d->I_s, 1),
+                                        moe::grouped_gemm_partial_bytes(1, T, d->H, 0))
                              : 0;
+  L.ctr_main = take(moe::grouped_gemm_counter_region_bytes());
+  L.ctr_side = take(moe::grouped_gemm_counter_region_bytes());
+  L.route_ticket = take(sizeof(unsigned int));
   L.gemm_main = take(L.gemm_main_bytes);
   L.gemm_side = take(L.gemm_side_bytes);
   L.logits = take(moe::route_ws_bytes(T, d->H, d->E));
@@ -126,7 +135,7 @@ extern "C" {
 
 size_t moe_route_workspace_bytes(int T, int H, int E) {
   if (T < 0 || H <= 0 || E <= 0) return 0;
-  return moe::route_ws_bytes(T, H, E);
+  return kRouteTicketBytes + moe::route_ws_bytes(T, H, E);
 }
 
 int moe_route(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
@@ -139,12 +148,18 @@ int moe_route(const void* x, const float* w_router, const float* bias, int T, in
   if (!al16(x) || !al16(w_router) || !al16(ws) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
       (reinterpret_cast<uintptr_t>(topk_w) & 3u) || (reinterpret_cast<uintptr_t>(bias) & 3u))
     return MOE_ERR_UNSUPPORTED;
-  if (ws_bytes < moe::route_ws_bytes(T, H, E)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < kRouteTicketBytes + moe::route_ws_bytes(T, H, E)) return MOE_ERR_WORKSPACE;
   DevInfo* di = nullptr;
   int rc = dev_info(&di);
   if (rc) return rc;
   int n = 0;
-  rc = moe::route_launch(x, w_router, bias, T, H, E, k, topk_ids, topk_w, static_cast<float*>(ws), nullptr,
+  // ws = [ticket counter | logits scratch]; the counter is cleared here, so ws
+  // may hold anything on entry
+  unsigned int* ticket = static_cast<unsigned int*>(ws);
+  if (T <= moe::route_small_max_tokens() && cudaMemsetAsync(ticket, 0, sizeof(unsigned int), stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  rc = moe::route_launch(x, w_router, bias, T, H, E, k, topk_ids, topk_w,
+                         reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kRouteTicketBytes), ticket, nullptr,
                          di->status, di->sms, stream, &n);
   t_last_launches = n;
   return rc;
@@ -199,7 +214,8 @@ int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets,
   if (rc) return rc;
   if (ws && ws_bytes < moe::grouped_gemm_ws_bytes(G, rows_max, N, act)) return MOE_ERR_WORKSPACE;
   int n = 0;
-  rc = moe::grouped_gemm_launch(a, w, group_offsets, G, rows_max, N, K, act, out, di->status, ws, ws_bytes, di->sms,
+  const moe::GemmScratch scratch = moe::grouped_gemm_scratch(ws, ws_bytes);
+  rc = moe::grouped_gemm_launch(a, w, group_offsets, G, rows_max, N, K, act, out, di->status, &scratch, di->sms,
                                 stream, &n);
   t_last_launches = n;
   return rc;
@@ -259,8 +275,8 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
   void* hs = base + L.hs;
   void* s = base + L.s;
   void* xperm = base + L.xperm;
-  void* gmain = base + L.gemm_main;
-  void* gside = base + L.gemm_side;
+  const moe::GemmScratch gmain{reinterpret_cast<int*>(base + L.ctr_main), base + L.gemm_main, L.gemm_main_bytes};
+  const moe::GemmScratch gside{reinterpret_cast<int*>(base + L.ctr_side), base + L.gemm_side, L.gemm_side_bytes};
   const int rows = T * d->k;
   int n = 0;
 
@@ -269,29 +285,30 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
     if (!has_shared) return MOE_OK;
     if (cudaEventRecord(ev_fork, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamWaitEvent(side, ev_fork, 0) != cudaSuccess) return MOE_ERR_CUDA;
-    int r = moe::grouped_gemm_launch(x, w->ws_gate_up, nullptr, 1, T, d->I_s, d->H, 1, hs, di->status, gside,
-                                     L.gemm_side_bytes, di->sms, side, &n);
+    int r = moe::grouped_gemm_launch(x, w->ws_gate_up, nullptr, 1, T, d->I_s, d->H, 1, hs, di->status, &gside,
+                                     di->sms, side, &n);
     if (!r)
-      r = moe::grouped_gemm_launch(hs, w->ws_down, nullptr, 1, T, d->H, d->I_s, 0, s, di->status, gside,
-                                   L.gemm_side_bytes, di->sms, side, &n);
+      r = moe::grouped_gemm_launch(hs, w->ws_down, nullptr, 1, T, d->H, d->I_s, 0, s, di->status, &gside,
+                                   di->sms, side, &n);
     if (r) return r;
     return cudaEventRecord(ev_join, side) != cudaSuccess ? MOE_ERR_CUDA : MOE_OK;
   };
   // routed path on `stream`: route -> dispatch -> gmm1 (+SiLU*mul) -> gmm2
   if (T <= moe::route_small_max_tokens()) {
-    // decode sizes: the shared expert streams its weights while one small
-    // cluster routes and dispatches
+    // decode sizes: the shared expert streams its weights while one router
+    // launch routes and dispatches
     rc = fork_shared();
     // router, top-k and counting sort in one launch
-    const moe::DispatchOut dout{offsets, sorted, inv, nullptr};
+    const moe::DispatchOut dout{offsets, sorted, inv};
     if (!rc)
-      rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, &dout,
-                             di->status, di->sms, stream, &n);
+      rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits,
+                             reinterpret_cast<unsigned int*>(base + L.route_ticket), &dout, di->status, di->sms,
+                             stream, &n);
   } else {
     if (kForkStage == 0) rc = fork_shared();
     if (!rc)
       rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, nullptr,
-                             di->status, di->sms, stream, &n);
+                             nullptr, di->status, di->sms, stream, &n);
     if (!rc && kForkStage == 1) rc = fork_shared();
     if (!rc)
       rc = moe::permute_launch(ids, x, T, d->H, d->E, d->k, offsets, sorted, inv, xperm, pcounts, di->status,
@@ -304,13 +321,13 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
     // permuted copy, since one producer thread issuing a gather per 4 rows
     // cannot feed full 128-row tiles
     rc = T <= moe::route_small_max_tokens()
-             ? moe::grouped_gemm_launch(x, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, gmain,
-                                        L.gemm_main_bytes, di->sms, stream, &n, sorted, T)
+             ? moe::grouped_gemm_launch(x, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, &gmain,
+                                        di->sms, stream, &n, sorted, T)
              : moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status,
-                                        gmain, L.gemm_main_bytes, di->sms, stream, &n);
+                                        &gmain, di->sms, stream, &n);
   if (!rc)
-    rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, gmain,
-                                  L.gemm_main_bytes, di->sms, stream, &n);
+    rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, &gmain,
+                                  di->sms, stream, &n);
   if (rc) return rc;
   // join, then combine
   if (has_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;

@@ -688,30 +688,34 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 struct SplitPlan {
   int unit_cap = 0;
   int split_cap = 0;
-  size_t counter_bytes = 0;
-  size_t bytes = 0;
+  size_t partial_bytes = 0;   // 0: the launch never splits
 };
 
 constexpr int kSwapRows = 64;   // token rows per unit in the weights-on-M form
 constexpr int kMaxSlots = 4096;
+// Ticket counters: a fixed region at the start of every split-K scratch, the
+// same size whatever the shape, so that calls of different shapes can share a
+// scratch in turn (no call's partial sums ever land where another call keeps
+// its counters).  Units beyond it are never split.
+constexpr int kCounterInts = 16384;
 
 SplitPlan split_plan(int G, int rows_max, int N, int act, int max_slots = kMaxSlots) {
   SplitPlan p;
   if (rows_max <= 0 || N % 128 || static_cast<long long>(rows_max) > 64LL * G) return p;
   const long long nonempty = G < rows_max ? G : rows_max;
-  const long long units = ((rows_max + kSwapRows - 1) / kSwapRows + nonempty) * (N / 128);
+  long long units = ((rows_max + kSwapRows - 1) / kSwapRows + nonempty) * (N / 128);
+  if (units > kCounterInts) units = kCounterInts;
   const long long cap = units * kMaxSplit < max_slots ? units * kMaxSplit : max_slots;
   p.unit_cap = static_cast<int>(units);
   p.split_cap = static_cast<int>(cap);
-  p.counter_bytes = align_up(static_cast<size_t>(units) * sizeof(int));
   const size_t slot = 128 * static_cast<size_t>(act ? partial_floats<1>() : partial_floats<0>()) * sizeof(float);
-  p.bytes = p.counter_bytes + static_cast<size_t>(cap) * slot;
+  p.partial_bytes = static_cast<size_t>(cap) * slot;
   return p;
 }
 
 template <int SWAP, int W, int ACT>
 int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K, void* out,
-               int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream, int* launches,
+               int* status, const GemmScratch* scratch, int grid_cap, cudaStream_t stream, int* launches,
                int max_slots = kMaxSlots, int K_a = 0, const int32_t* a_rows = nullptr, int a_src_rows = 0) {
   using C = Cfg<SWAP, W, ACT>;
   static bool attr_done[64] = {};
@@ -739,11 +743,11 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
       (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) * (N / C::kOutCols);
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
                 nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows};
-  if (SWAP && ws) {
+  if (SWAP && scratch && scratch->counters && scratch->partials) {
     const SplitPlan p = split_plan(G, rows_max, N, ACT, max_slots);
-    if (p.bytes && ws_bytes >= p.bytes) {
-      args.counters = static_cast<int*>(ws);
-      args.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + p.counter_bytes);
+    if (p.partial_bytes && scratch->partial_bytes >= p.partial_bytes) {
+      args.counters = scratch->counters;
+      args.partials = static_cast<float*>(scratch->partials);
       args.unit_cap = p.unit_cap;
       args.split_cap = p.split_cap;
       bound *= kMaxSplit;
@@ -764,58 +768,59 @@ bool grouped_gemm_weights_on_m(int G, int rows_max, int N) {
   return N % 128 == 0 && static_cast<long long>(rows_max) <= 64LL * G;
 }
 
-size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act) {
-  return split_plan(G, rows_max, N, act).bytes;
+size_t grouped_gemm_counter_region_bytes() { return static_cast<size_t>(kCounterInts) * sizeof(int); }
+
+size_t grouped_gemm_partial_bytes(int G, int rows_max, int N, int act, int max_slots) {
+  return split_plan(G, rows_max, N, act, max_slots > 0 ? max_slots : kMaxSlots).partial_bytes;
+}
+
+size_t grouped_gemm_counters_used_bytes(int G, int rows_max, int N, int act) {
+  return align_up(static_cast<size_t>(split_plan(G, rows_max, N, act).unit_cap) * sizeof(int));
+}
+
+size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act, int max_slots) {
+  const size_t pb = grouped_gemm_partial_bytes(G, rows_max, N, act, max_slots);
+  return pb ? grouped_gemm_counter_region_bytes() + pb : 0;
+}
+
+GemmScratch grouped_gemm_scratch(void* ws, size_t ws_bytes) {
+  GemmScratch s{};
+  const size_t c = grouped_gemm_counter_region_bytes();
+  if (ws && ws_bytes > c) {
+    s.counters = static_cast<int*>(ws);
+    s.partials = static_cast<uint8_t*>(ws) + c;
+    s.partial_bytes = ws_bytes - c;
+  }
+  return s;
 }
 
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
-                        int act, void* out, int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream,
-                        int* launches, const int32_t* a_rows, int a_src_rows) {
+                        int act, void* out, int* status, const GemmScratch* scratch, int grid_cap, cudaStream_t stream,
+                        int* launches, const int32_t* a_rows, int a_src_rows, int max_slots) {
   if (rows_max == 0) return MOE_OK;
+  if (max_slots <= 0) max_slots = kMaxSlots;
   if (grouped_gemm_weights_on_m(G, rows_max, N)) {
     if (act == 1)
-      return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap,
-                                         stream, launches, kMaxSlots, 0, a_rows, a_src_rows);
-    return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap, stream,
-                                       launches, kMaxSlots, 0, a_rows, a_src_rows);
+      return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,
+                                         launches, max_slots, 0, a_rows, a_src_rows);
+    return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,
+                                       launches, max_slots, 0, a_rows, a_src_rows);
   }
   if (act == 1) {
     if (N % 128 == 0)
-      return launch_cfg<0, 256, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
+      return launch_cfg<0, 256, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
                                    launches, kMaxSlots, 0, a_rows, a_src_rows);
-    return launch_cfg<0, 128, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
-                                 launches, kMaxSlots, 0, a_rows, a_src_rows);
+    return launch_cfg<0, 128, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream, launches,
+                                 kMaxSlots, 0, a_rows, a_src_rows);
   }
   if (N % 256 == 0)
-    return launch_cfg<0, 256, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
-                                 launches, kMaxSlots, 0, a_rows, a_src_rows);
+    return launch_cfg<0, 256, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream, launches,
+                                 kMaxSlots, 0, a_rows, a_src_rows);
   if (N % 128 == 0)
-    return launch_cfg<0, 128, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream,
-                                 launches, kMaxSlots, 0, a_rows, a_src_rows);
-  return launch_cfg<0, 64, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, 0, grid_cap, stream, launches,
+    return launch_cfg<0, 128, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream, launches,
+                                 kMaxSlots, 0, a_rows, a_src_rows);
+  return launch_cfg<0, 64, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream, launches,
                               kMaxSlots, 0, a_rows, a_src_rows);
-}
-
-size_t grouped_gemm_counter_bytes(int G, int rows_max, int N, int act) {
-  return split_plan(G, rows_max, N, act).counter_bytes;
-}
-
-size_t grouped_gemm_ws_bytes_slots(int G, int rows_max, int N, int act, int max_slots) {
-  return split_plan(G, rows_max, N, act, max_slots).bytes;
-}
-
-int grouped_gemm_launch_slots(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
-                              int act, void* out, int* status, void* ws, size_t ws_bytes, int max_slots, int grid_cap,
-                              cudaStream_t stream, int* launches) {
-  if (rows_max == 0) return MOE_OK;
-  if (!grouped_gemm_weights_on_m(G, rows_max, N))
-    return grouped_gemm_launch(a, w, offsets, G, rows_max, N, K, act, out, status, nullptr, 0, grid_cap, stream,
-                               launches);
-  if (act == 1)
-    return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap, stream,
-                                       launches, max_slots);
-  return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, ws, ws_bytes, grid_cap, stream,
-                                     launches, max_slots);
 }
 
 int router_gemm_launch(const void* x, const void* wr3, int T, int H, int E, float* logits, int* status, int grid_cap,
@@ -825,12 +830,12 @@ int router_gemm_launch(const void* x, const void* wr3, int T, int H, int E, floa
   // narrower N blocks while the row blocks alone would leave SMs idle
   const long long mtiles = (T + 127) / 128;
   if (E % 256 == 0 && mtiles * (E / 256) >= grid_cap)
-    return launch_cfg<0, 256, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, 0, grid_cap, stream, launches,
+    return launch_cfg<0, 256, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, grid_cap, stream, launches,
                                  kMaxSlots, H);
   if (E % 128 == 0 && mtiles * (E / 128) >= grid_cap)
-    return launch_cfg<0, 128, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, 0, grid_cap, stream, launches,
+    return launch_cfg<0, 128, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, grid_cap, stream, launches,
                                  kMaxSlots, H);
-  return launch_cfg<0, 64, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, 0, grid_cap, stream, launches,
+  return launch_cfg<0, 64, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, grid_cap, stream, launches,
                               kMaxSlots, H);
 }
 

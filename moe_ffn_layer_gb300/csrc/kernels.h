@@ -14,15 +14,16 @@ struct DispatchOut {
   int32_t* offsets;
   int32_t* sorted_token;
   int32_t* inv_perm;
-  void* x_perm;   // may be nullptr
 };
 
 size_t route_ws_bytes(int T, int H, int E);
 int route_small_max_tokens();
+// logits_ws: route_ws_bytes(T, H, E) bytes.  ticket: a counter that is zero on
+// entry and left zero (used for T <= route_small_max_tokens(), required there).
 // dispatch != nullptr requires T <= route_small_max_tokens().
 int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
-                 int32_t* topk_ids, float* topk_w, float* logits_ws, const DispatchOut* dispatch, int* status,
-                 int grid_cap, cudaStream_t stream, int* launches);
+                 int32_t* topk_ids, float* topk_w, float* logits_ws, unsigned int* ticket, const DispatchOut* dispatch,
+                 int* status, int grid_cap, cudaStream_t stream, int* launches);
 
 size_t permute_ws_bytes(int T, int E);
 int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, int k, int32_t* offsets,
@@ -30,21 +31,30 @@ int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, 
                    int num_sms, cudaStream_t stream, int* launches);
 
 bool grouped_gemm_weights_on_m(int G, int rows_max, int N);
-// Split-K scratch bytes of a launch (0: never splits).
-size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act);
-// ws (nullable): split-K scratch, zero-filled before its first use; left zero.
+// Split-K scratch of the weights-on-M form: ticket counters (zero between
+// calls; every call leaves the ones it used zero) and partial-sum slots.
+struct GemmScratch {
+  int* counters;          // grouped_gemm_counter_region_bytes() bytes, or nullptr: no split
+  void* partials;
+  size_t partial_bytes;
+};
+// Size of the counter region, the same for every shape.
+size_t grouped_gemm_counter_region_bytes();
+// Counter bytes (from the start of the region) a launch of this shape may use.
+size_t grouped_gemm_counters_used_bytes(int G, int rows_max, int N, int act);
+// Partial-slot bytes a launch needs to split with at most max_slots slots (0: default cap);
+// 0 when the shape never splits.
+size_t grouped_gemm_partial_bytes(int G, int rows_max, int N, int act, int max_slots = 0);
+// One buffer laid out as [counter region | partial slots]; 0 when the shape never splits.
+size_t grouped_gemm_ws_bytes(int G, int rows_max, int N, int act, int max_slots = 0);
+GemmScratch grouped_gemm_scratch(void* ws, size_t ws_bytes);
+// scratch (nullable): split-K scratch.
 // a_rows (nullable): token row r of the product is row a_rows[r] of `a`, a
 // [a_src_rows][K] tensor (rows fetched by TMA gather4, no permuted copy).
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
-                        int act, void* out, int* status, void* ws, size_t ws_bytes, int grid_cap, cudaStream_t stream,
-                        int* launches, const int32_t* a_rows = nullptr, int a_src_rows = 0);
-// Bytes at the start of the split-K scratch that hold the ticket counters.
-size_t grouped_gemm_counter_bytes(int G, int rows_max, int N, int act);
-// The same with at most max_slots split-K partial slots (a smaller scratch).
-size_t grouped_gemm_ws_bytes_slots(int G, int rows_max, int N, int act, int max_slots);
-int grouped_gemm_launch_slots(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
-                              int act, void* out, int* status, void* ws, size_t ws_bytes, int max_slots, int grid_cap,
-                              cudaStream_t stream, int* launches);
+                        int act, void* out, int* status, const GemmScratch* scratch, int grid_cap,
+                        cudaStream_t stream, int* launches, const int32_t* a_rows = nullptr, int a_src_rows = 0,
+                        int max_slots = 0);
 int grouped_gemm_max_groups();
 // logits[T][E] fp32 = x[T][H] . (hi + mid + lo)^T with wr3 = bf16 [E][3H] holding
 // the three bf16 terms of the fp32 router weights in K order (hi | mid | lo);

@@ -55,7 +55,7 @@ int moe_grouped_gemm_noalloc(const void* a, const void* w, const int32_t* group_
   if (!al16(a) || !al16(w) || !al16(out) || (reinterpret_cast<uintptr_t>(group_offsets) & 3u))
     return MOE_ERR_UNSUPPORTED;
   // problems whose split-K scratch does not fit the fixed array are refused
-  const size_t need = moe::grouped_gemm_ws_bytes_slots(G, rows_max, N, act, kScratchSlots);
+  const size_t need = moe::grouped_gemm_ws_bytes(G, rows_max, N, act, kScratchSlots);
   if (need > kScratchBytes) return MOE_ERR_WORKSPACE;
   int* status = nullptr;
   int sms = 0;
@@ -64,13 +64,15 @@ int moe_grouped_gemm_noalloc(const void* a, const void* w, const int32_t* group_
   void* scratch = nullptr;
   rc = scratch_address(&scratch);
   if (rc) return rc;
-  // the array keeps whatever the previous call left: the ticket counters must
-  // start at zero, so clear them (the partial slots are always written first)
-  const size_t counters = moe::grouped_gemm_counter_bytes(G, rows_max, N, act);
+  // the array keeps whatever the previous call left: the ticket counters this
+  // launch may use must start at zero, so clear them (the partial slots are
+  // always written before they are read)
+  const size_t counters = moe::grouped_gemm_counters_used_bytes(G, rows_max, N, act);
   if (need && counters && cudaMemsetAsync(scratch, 0, counters, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  const moe::GemmScratch s = moe::grouped_gemm_scratch(scratch, kScratchBytes);
   int n = 0;
-  return moe::grouped_gemm_launch_slots(a, w, group_offsets, G, rows_max, N, K, act, out, status, scratch,
-                                        kScratchBytes, kScratchSlots, sms, stream, &n);
+  return moe::grouped_gemm_launch(a, w, group_offsets, G, rows_max, N, K, act, out, status, &s, sms, stream, &n,
+                                  nullptr, 0, kScratchSlots);
 }
 
 }  // extern "C"

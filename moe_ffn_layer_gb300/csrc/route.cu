@@ -10,14 +10,11 @@
 // definition in its benchmark shapes.
 //
 // Kernels:
-//   T <= 16   route_small: one 8-CTA thread-block cluster does the whole
-//             router (and, inside the layer forward, the dispatch too): each
-//             warp streams one (expert, H slice) of Wr once and dots it with
-//             every token; partial logits go to CTA 0's shared memory through
-//             distributed shared memory; after a cluster barrier CTA 0 adds
-//             them in slice order, takes the top-k, and (optionally) runs the
-//             counting sort; after a second barrier all CTAs gather the rows.
-//             Decode shapes: one launch instead of four, no global counters.
+//   T <= 16   route_small: one warp per (expert, 512-wide slice of H)
+//             streams its slice of Wr once and dots it with every token; the
+//             CTA that finishes last (a ticket counter) adds the slices in
+//             slice order, takes the top-k and, inside the layer forward, runs
+//             the counting sort as well.  Decode shapes: one launch.
 //   T >  16   logits, then topk_softmax (one warp per token; adds the bias).
 //             Logits for T >= 512 (E, H multiples of 64) come from the tensor
 //             cores: each fp32 weight is split exactly into three bf16 terms
@@ -28,12 +25,8 @@
 //             adds them in fp32 with K = 3H.  Fewer tokens: fp32 FMAs, one
 //             warp per (expert, 16 tokens) below 512 tokens, else a 64 x 64
 //             SIMT tile GEMM.
-#include <cooperative_groups.h>
-
 #include "common.cuh"
 #include "kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace moe {
 namespace {
@@ -156,13 +149,14 @@ __global__ void __launch_bounds__(256)
 // chosen k, the sum taken by a fixed butterfly.  Registers only.
 //
 // Refinement (logits from the tensor cores, refine != nullptr): if the k-th
-// and (k+1)-th logits lie within kRefineDelta, every expert whose logit lies
+// and (k+1)-th logits lie within kRefineDelta (5e-4, at least 8x the
+// tensor-core logit error measured at these sizes), every expert whose logit lies
 // within kRefineDelta of the k-th is re-evaluated with fp32 FMAs (x . Wr[e] +
 // b[e]) and the selection is run again.  The tensor-core logits differ from
 // fp32 ones by far less than kRefineDelta / 2, so experts outside that band
 // keep their side of the boundary and the choice equals the fp32 choice.
 constexpr int kTopkMaxPerLane = kMaxExperts / 32;
-constexpr float kRefineDelta = 1e-3f;
+constexpr float kRefineDelta = 5e-4f;
 
 struct Refine {
   const __nv_bfloat16* x;   // this token's row [H]
@@ -173,6 +167,7 @@ struct Refine {
 __device__ __forceinline__ float warp_dot_fp32(const __nv_bfloat16* x, const float* w, int H) {
   const int lane = threadIdx.x & 31;
   float acc = 0.f;
+#pragma unroll 4
   for (int h0 = lane * 8; h0 < H; h0 += 256) {
     const uint4 xv = *reinterpret_cast<const uint4*>(x + h0);
     const float4 w0 = *reinterpret_cast<const float4*>(w + h0);
@@ -302,139 +297,167 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// ---------------------------------------------------------------- T <= 16: one cluster
+// ---------------------------------------------------------------- T <= 16: one kernel
 
 constexpr int kSmallT = 16;
-constexpr int kClusterCtas = 8;
-constexpr int kSmallThreads = 1024;
-constexpr int kSmallWarps = kClusterCtas * kSmallThreads / 32;   // 256 warps in the cluster
+constexpr int kSliceH = 512;            // H elements per partial-logit warp
+constexpr int kSmallThreads = 256;
+constexpr int kMaxSlices = 8;           // at most this many H slices
 
 struct SmallArgs {
-  const __nv_bfloat16* x;
-  const float* wr;
-  const float* bias;
-  int T, H, E, k, S;          // S: H slices per expert
+  const __nv_bfloat16* x;     // [T][H]
+  const float* wr;            // [E][H]
+  const float* bias;          // [E] or nullptr
+  int T, H, E, k, S;
+  float* part;                // [S][T][E] partial logits
+  unsigned int* ticket;       // zero on entry; the last CTA sets it back to zero
   int32_t* topk_ids;
   float* topk_w;
   int32_t* offsets;           // nullptr: route only
   int32_t* sorted_token;
   int32_t* inv_perm;
-  __nv_bfloat16* x_perm;      // nullptr: no row gather
 };
 
-template <int NPL>
-__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kSmallThreads, 1)
-    route_small_kernel(const SmallArgs a) {
-  __shared__ float part[kSmallT * kMaxExperts];   // [S][T][E]; S * E <= max(256, E)
+// Every CTA: partial logits part[s][t][e] = sum over slice s of H of
+// x[t, h] * Wr[e, h], one warp per (expert, slice), lanes striding the slice
+// eight elements at a time (16-byte loads, all of a warp's loads in flight).
+// The CTA that arrives last (ticket) adds the slices in slice order (+ bias),
+// takes the top-k of every token (one warp per token) and, inside the layer
+// forward, runs the counting sort by (expert, token).
+// NT: token rows the GEMV carries (a power of two >= T); rows past T re-read
+// row T-1, so that every load of a step is issued unconditionally.
+template <int NPL, int NT>
+__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallArgs a) {
+  __shared__ float logit[kSmallT * kMaxExperts];
   __shared__ int32_t s_ids[kSmallT * kMaxTopK];
   __shared__ float s_w[kSmallT * kMaxTopK];
   __shared__ uint32_t s_mask[kMaxExperts];
   __shared__ int s_off[kMaxExperts];
-  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ int s_last;
   chain_wait();
   const ChainReleaseAtExit release_next;
-  const int rank = static_cast<int>(cluster.block_rank());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.T, H = a.H, E = a.E, k = a.k, S = a.S;
-  const int HS = H / S;
-  float* part0 = cluster.map_shared_rank(part, 0);
-
-  // ---- partial logits: warp task (e, s) dots Wr[e, s-th slice] with every token
-  for (int task = rank * (kSmallThreads / 32) + warp; task < E * S; task += kSmallWarps) {
-    const int e = task / S, sl = task % S;
-    float acc[kSmallT];
+  const int T = a.T, E = a.E, k = a.k, S = a.S;
+  const int gw = blockIdx.x * (kSmallThreads / 32) + warp;
+  if (gw < E * S) {
+    const int e = gw % E, sl = gw / E;
+    const int HS = a.H / S;
+    float acc[NT];
 #pragma unroll
-    for (int t = 0; t < kSmallT; ++t) acc[t] = 0.f;
-    const float* w = a.wr + static_cast<size_t>(e) * H;
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    const float* w = a.wr + static_cast<size_t>(e) * a.H;
 #pragma unroll 2
     for (int h0 = sl * HS + lane * 8; h0 < (sl + 1) * HS; h0 += 256) {
       const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + h0));
       const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + h0 + 4));
+      uint4 xv[NT];
 #pragma unroll
-      for (int t = 0; t < kSmallT; ++t) {
-        if (t < T) {
-          const uint4 xv = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * H + h0));
-          float f[8];
-          bf16x8_to_f32(xv, f);
-          float v = acc[t];
-          v = fmaf(f[0], w0.x, v); v = fmaf(f[1], w0.y, v); v = fmaf(f[2], w0.z, v); v = fmaf(f[3], w0.w, v);
-          v = fmaf(f[4], w1.x, v); v = fmaf(f[5], w1.y, v); v = fmaf(f[6], w1.z, v); v = fmaf(f[7], w1.w, v);
-          acc[t] = v;
-        }
-      }
-    }
+      for (int t = 0; t < NT; ++t)
+        xv[t] = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t < T ? t : T - 1) * a.H + h0));
 #pragma unroll
-    for (int t = 0; t < kSmallT; ++t) {
-      if (t < T) {
+      for (int t = 0; t < NT; ++t) {
+        float f[8];
+        bf16x8_to_f32(xv[t], f);
         float v = acc[t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) part0[(sl * T + t) * E + e] = v;
+        v = fmaf(f[0], w0.x, v); v = fmaf(f[1], w0.y, v); v = fmaf(f[2], w0.z, v); v = fmaf(f[3], w0.w, v);
+        v = fmaf(f[4], w1.x, v); v = fmaf(f[5], w1.y, v); v = fmaf(f[6], w1.z, v); v = fmaf(f[7], w1.w, v);
+        acc[t] = v;
       }
     }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == t && t < T) a.part[(static_cast<size_t>(sl) * T + t) * E + e] = v;
+    }
   }
-  cluster.sync();
+  // the last CTA to finish its partials goes on
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) *a.ticket = 0u;   // every CTA has taken its ticket
+  // slices added in slice order; every load of a thread goes out before the
+  // first add (slices past S re-read slice S-1 and are not added)
+  const size_t slice = static_cast<size_t>(T) * E;
+#pragma unroll 2
+  for (int i = threadIdx.x; i < T * E; i += kSmallThreads) {
+    float p[kMaxSlices];
+#pragma unroll
+    for (int sl = 0; sl < kMaxSlices; ++sl) p[sl] = __ldcg(a.part + (sl < S ? sl : S - 1) * slice + i);
+    const float b = a.bias ? __ldg(a.bias + i % E) : 0.f;
+    float v = p[0];
+#pragma unroll
+    for (int sl = 1; sl < kMaxSlices; ++sl)
+      if (sl < S) v += p[sl];
+    logit[i] = v + b;
+  }
+  if (a.offsets)
+    for (int e = threadIdx.x; e < E; e += kSmallThreads) s_mask[e] = 0;
+  __syncthreads();
+  for (int t = warp; t < T; t += kSmallThreads / 32)
+    warp_topk_softmax<NPL>(logit + t * E, nullptr, E, k, s_ids + t * k, s_w + t * k);
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += kSmallThreads) {
+    a.topk_ids[i] = s_ids[i];
+    a.topk_w[i] = s_w[i];
+    if (a.offsets) atomicOr(&s_mask[s_ids[i]], 1u << (i / k));   // token bitmask per expert
+  }
+  if (!a.offsets) return;
+  __syncthreads();
+  if (warp == 0) {   // exclusive scan of the counts over experts
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < E ? __popc(s_mask[e]) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (e < E) s_off[e] = run + incl - c;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) a.offsets[E] = run;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kSmallThreads) a.offsets[e] = s_off[e];
+  for (int i = threadIdx.x; i < T * k; i += kSmallThreads) {
+    const int t = i / k, e = s_ids[i];
+    const int r = s_off[e] + __popc(s_mask[e] & ((1u << t) - 1u));
+    a.sorted_token[r] = t;
+    a.inv_perm[i] = r;
+  }
+}
 
-  if (rank == 0) {
-    // ---- logits = slices added in order (+ bias), in place in slice 0
-    for (int i = threadIdx.x; i < T * E; i += kSmallThreads) {
-      float v = part[i];
-      for (int sl = 1; sl < S; ++sl) v += part[sl * T * E + i];
-      if (a.bias) v += a.bias[i % E];
-      part[i] = v;
-    }
-    __syncthreads();
-    if (warp < T) warp_topk_softmax<NPL>(part + warp * E, nullptr, E, k, s_ids + warp * k, s_w + warp * k);
-    __syncthreads();
-    for (int i = threadIdx.x; i < T * k; i += kSmallThreads) {
-      a.topk_ids[i] = s_ids[i];
-      a.topk_w[i] = s_w[i];
-    }
-    if (a.offsets) {
-      // ---- counting sort by (expert, token): token bitmask per expert
-      for (int e = threadIdx.x; e < E; e += kSmallThreads) s_mask[e] = 0;
-      __syncthreads();
-      for (int i = threadIdx.x; i < T * k; i += kSmallThreads) atomicOr(&s_mask[s_ids[i]], 1u << (i / k));
-      __syncthreads();
-      if (warp == 0) {   // exclusive scan of the counts over experts
-        int run = 0;
-        for (int e0 = 0; e0 < E; e0 += 32) {
-          const int e = e0 + lane;
-          const int c = e < E ? __popc(s_mask[e]) : 0;
-          int incl = c;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
-          }
-          if (e < E) s_off[e] = run + incl - c;
-          run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) a.offsets[E] = run;
-      }
-      __syncthreads();
-      for (int e = threadIdx.x; e < E; e += kSmallThreads) a.offsets[e] = s_off[e];
-      for (int i = threadIdx.x; i < T * k; i += kSmallThreads) {
-        const int t = i / k, e = s_ids[i];
-        const int r = s_off[e] + __popc(s_mask[e] & ((1u << t) - 1u));
-        a.sorted_token[r] = t;
-        a.inv_perm[i] = r;
-      }
-    }
+template <int NPL>
+cudaError_t launch_small_nt(int nt, int grid, cudaStream_t stream, const SmallArgs& a) {
+  const dim3 g(grid), b(kSmallThreads);
+  switch (nt) {
+    case 1: return launch_chained(route_small_kernel<NPL, 1>, g, b, 0, stream, a);
+    case 2: return launch_chained(route_small_kernel<NPL, 2>, g, b, 0, stream, a);
+    case 4: return launch_chained(route_small_kernel<NPL, 4>, g, b, 0, stream, a);
+    case 8: return launch_chained(route_small_kernel<NPL, 8>, g, b, 0, stream, a);
+    default: return launch_chained(route_small_kernel<NPL, 16>, g, b, 0, stream, a);
   }
-  if (a.x_perm) {
-    // the barrier's release/acquire makes CTA 0's sorted_token stores visible
-    cluster.sync();
-    // ---- row gather: x_perm[r] = x[sorted[r]], one warp per row across the cluster
-    const int vec = H / 8;
-    for (int r = rank * (kSmallThreads / 32) + warp; r < T * k; r += kSmallWarps) {
-      const int t = a.sorted_token[r];
-      const uint4* src = reinterpret_cast<const uint4*>(a.x) + static_cast<size_t>(t) * vec;
-      uint4* dst = reinterpret_cast<uint4*>(a.x_perm) + static_cast<size_t>(r) * vec;
-      for (int i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
-    }
-  }
-  // other CTAs touch CTA 0's shared memory only before the first barrier
+}
+
+cudaError_t launch_small(int npl, int nt, int grid, cudaStream_t stream, const SmallArgs& a) {
+  if (npl == 4) return launch_small_nt<4>(nt, grid, stream, a);
+  if (npl == 8) return launch_small_nt<8>(nt, grid, stream, a);
+  return launch_small_nt<16>(nt, grid, stream, a);
+}
+
+int small_slices(int H) {
+  int S = H / kSliceH;
+  if (S < 1) S = 1;
+  if (S > kMaxSlices) S = kMaxSlices;
+  while (S > 1 && H % (S * 8)) --S;
+  return S;
 }
 
 }  // namespace
@@ -444,7 +467,7 @@ constexpr int kTcMinT = 512;   // from this many tokens the logits come from the
 bool route_uses_tc(int T, int H, int E) { return T >= kTcMinT && E % 64 == 0 && H % 64 == 0; }
 
 size_t route_ws_bytes(int T, int H, int E) {
-  size_t b = align_up(static_cast<size_t>(T) * E * sizeof(float));
+  size_t b = align_up(static_cast<size_t>(T) * E * sizeof(float) * (T <= kSmallT ? small_slices(H) : 1));
   if (route_uses_tc(T, H, E)) b += align_up(static_cast<size_t>(E) * 3 * H * 2);
   return b;
 }
@@ -452,29 +475,23 @@ size_t route_ws_bytes(int T, int H, int E) {
 int route_small_max_tokens() { return kSmallT; }
 
 int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
-                 int32_t* topk_ids, float* topk_w, float* logits_ws, const DispatchOut* dispatch, int* status,
-                 int grid_cap, cudaStream_t stream, int* launches) {
+                 int32_t* topk_ids, float* topk_w, float* logits_ws, unsigned int* ticket, const DispatchOut* dispatch,
+                 int* status, int grid_cap, cudaStream_t stream, int* launches) {
   if (T == 0) return MOE_OK;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (T <= kSmallT) {
-    int S = kSmallWarps / E;
-    if (S < 1) S = 1;
-    while (S > 1 && H % (S * 8)) --S;
-    SmallArgs a{xb, w_router, bias, T, H, E, k, S, topk_ids, topk_w, nullptr, nullptr, nullptr, nullptr};
+    if (!ticket) return MOE_ERR_INVALID;
+    const int S = small_slices(H);
+    const int grid = (E * S + kSmallThreads / 32 - 1) / (kSmallThreads / 32);
+    SmallArgs a{xb, w_router, bias, T, H, E, k, S, logits_ws, ticket, topk_ids, topk_w, nullptr, nullptr, nullptr};
     if (dispatch) {
       a.offsets = dispatch->offsets;
       a.sorted_token = dispatch->sorted_token;
       a.inv_perm = dispatch->inv_perm;
-      a.x_perm = static_cast<__nv_bfloat16*>(dispatch->x_perm);
     }
-    cudaError_t rc;
-    if (E <= 128)
-      rc = launch_chained(route_small_kernel<4>, dim3(kClusterCtas), dim3(kSmallThreads), 0, stream, a);
-    else if (E <= 256)
-      rc = launch_chained(route_small_kernel<8>, dim3(kClusterCtas), dim3(kSmallThreads), 0, stream, a);
-    else
-      rc = launch_chained(route_small_kernel<16>, dim3(kClusterCtas), dim3(kSmallThreads), 0, stream, a);
-    if (rc != cudaSuccess) return MOE_ERR_CUDA;
+    const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
+    const int npl = E <= 128 ? 4 : E <= 256 ? 8 : 16;
+    if (launch_small(npl, nt, grid, stream, a) != cudaSuccess) return MOE_ERR_CUDA;
     ++*launches;
     return MOE_OK;
   }

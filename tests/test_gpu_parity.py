@@ -249,6 +249,36 @@ def test_grouped_gemm_single_group_no_offsets(T, N, K, act):
     assert_close_layer(to_f64(out), ref, "single group")
 
 
+def test_grouped_gemm_shapes_share_one_scratch():
+    """Calls of different shapes use one scratch buffer in turn (sized for the
+    largest); each gives the same bits as with a fresh zeroed scratch.  The
+    second shape has more units than the first and splits too, so its ticket
+    counters would sit where the first call left partial sums if the counter
+    region depended on the shape."""
+    seq = [([1, 2, 3, 1], 256, 2048, 1), ([1] * 40, 256, 2048, 0), ([1, 0, 3, 16, 2, 0, 9, 1], 384, 2048, 0),
+           ([2] * 30, 128, 1024, 1), ([1, 2, 3, 1], 256, 2048, 1)]
+    probs = []
+    for i, (rows, N, K, act) in enumerate(seq):
+        G = len(rows)
+        off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+        R = int(off[-1])
+        a = bf16_tensor(synth.random_bf16((R, K), seed=R + N + i, tag=55), "cuda")
+        w = bf16_tensor(synth.random_bf16((G, 2 * N if act else N, K), seed=K + G, tag=56, sigma=0.03), "cuda")
+        probs.append((a, w, i32(off), G, R, N, K, act))
+    big = max(B.moe_grouped_gemm_workspace_bytes(G, R, N, K, act) for _, _, _, G, R, N, K, act in probs)
+    shared = torch.zeros(big, dtype=torch.uint8, device="cuda")
+    for a, w, off, G, R, N, K, act in probs:
+        out = torch.empty((R, N), dtype=torch.bfloat16, device="cuda")
+        B.moe_grouped_gemm(a, w, off, G, R, N, K, act, out, shared, big, stream())
+        no_device_error()
+        nb = B.moe_grouped_gemm_workspace_bytes(G, R, N, K, act)
+        fresh = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
+        ref = torch.empty_like(out)
+        B.moe_grouped_gemm(a, w, off, G, R, N, K, act, ref, fresh, nb, stream())
+        no_device_error()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (G, R, N, K, act)
+
+
 def test_grouped_gemm_rejects_bad_offsets():
     """Offsets past rows_max or decreasing: the kernel records a device check
     error and computes nothing."""
@@ -373,6 +403,25 @@ def test_forward_without_shared_expert():
     out = L.forward(bf16_tensor(inp["x"], "cuda"))
     no_device_error()
     assert_close_layer(to_f64(out), ref["out"], "no shared expert")
+
+
+def test_forward_batches_of_different_sizes_share_one_workspace():
+    """One layer object keeps one workspace (sized for its largest batch) and
+    runs batches of different sizes in turn, across both router paths and both
+    tile forms; each output has the same bits as the same batch run through a
+    fresh workspace."""
+    wl = synth.Workload("vary", 300, 512, 16, 4, 1024, 128, sigma_router=0.1, sigma_w=0.03)
+    inp = synth.make_inputs(wl, 21)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    x = bf16_tensor(inp["x"], "cuda")
+    L.workspace(wl.T)
+    for T in [300, 8, 64, 1, 16, 200, 8, 3]:
+        got = L.forward(x[:T]).clone()
+        no_device_error()
+        fresh = MoEFFN.from_inputs(inp, wl.k, "cuda")
+        ref = fresh.forward(x[:T])
+        no_device_error()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), T
 
 
 def test_forward_repeatable_and_launch_count():

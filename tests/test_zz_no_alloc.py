@@ -32,6 +32,7 @@ CASES = [
     ([1, 2, 0, 1, 3, 1, 0, 2, 1, 1, 4, 0, 1, 2, 1, 1], 2048, 768, 0),
     ([8] * 16, 384, 1024, 1),
     ([300, 0, 129], 256, 192, 1),
+    ([1] * 64, 2048, 768, 0),   # 1024 units of one row each
 ]
 
 
@@ -61,10 +62,18 @@ def test_noalloc_matches_grouped_gemm(rows, N, K, act):
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
 
-def test_noalloc_refuses_problems_beyond_its_scratch():
-    """A problem whose split-K scratch would exceed the fixed array is refused
-    before anything is launched (pointers below are never dereferenced)."""
+def test_noalloc_refuses_bad_arguments_before_launch():
+    """Argument errors are refused on the host, before anything is launched
+    (the pointers below are never dereferenced)."""
     fake = 1 << 20
-    with pytest.raises(B.MoEError) as e:
-        B.moe_grouped_gemm_noalloc(fake, fake, fake, 1024, 65536, 262144, 64, 1, fake, None)
-    assert e.value.code == -3
+    for args, code in [
+        ((fake, fake, fake, 0, 16, 256, 64, 1, fake, None), -1),       # no groups
+        ((fake, fake, None, 4, 16, 256, 64, 1, fake, None), -1),       # several groups need offsets
+        ((fake, fake, fake, 4, 16, 200, 64, 1, fake, None), -2),       # N not a multiple of 64
+        ((fake, fake, fake, 4, 16, 256, 96, 1, fake, None), -2),       # K not a multiple of 64
+        ((fake + 8, fake, fake, 4, 16, 256, 64, 1, fake, None), -2),   # A not 16-byte aligned
+    ]:
+        with pytest.raises(B.MoEError) as e:
+            B.moe_grouped_gemm_noalloc(*args)
+        assert e.value.code == code, args
+
