@@ -11,8 +11,8 @@
 // Determinism: within a block of 256 tokens, the pairs of expert e form a
 // 256-bit mask indexed by token (atomicOr, order-free).  The rank of pair
 // (t, e) among the block's pairs of e is the popcount of the mask bits below
-// t; adding the block's base (an exclusive scan over blocks, then over
-// experts) gives the row.  Nothing depends on thread scheduling.
+// t; adding the block's base (the pairs of e in earlier blocks plus the pairs
+// of smaller experts) gives the row.  Nothing depends on thread scheduling.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -139,77 +139,46 @@ __global__ void __launch_bounds__(kTB)
   for (int e = tl; e < E; e += kTB) block_counts[static_cast<size_t>(blockIdx.x) * E + e] = mask_count(mask, e);
 }
 
-// Large T, pass 2 (one block of kScanThreads): block_counts[b][e] -> first row
-// of block b's pairs of expert e; offsets[e] = exclusive scan of the expert
-// totals.  One warp per expert scans its column of block counts.
-constexpr int kScanThreads = 1024;
-
-__global__ void __launch_bounds__(kScanThreads)
-    permute_scan_kernel(int32_t* __restrict__ block_counts, int B, int E, int32_t* __restrict__ offsets) {
-  __shared__ int s_tot[kMaxExperts];
-  __shared__ int s_off[kMaxExperts];
-  chain_wait();
-  const ChainReleaseAtExit release_next;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += kScanThreads / 32) {
-    int run = 0;
-    for (int b0 = 0; b0 < B; b0 += 32) {
-      const int b = b0 + lane;
-      const int c = b < B ? block_counts[static_cast<size_t>(b) * E + e] : 0;
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      if (b < B) block_counts[static_cast<size_t>(b) * E + e] = run + incl - c;
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) s_tot[e] = run;
-  }
-  __syncthreads();
-  if (warp == 0) {   // exclusive scan of the totals over experts
-    int run = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + lane;
-      const int c = e < E ? s_tot[e] : 0;
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      if (e < E) s_off[e] = run + incl - c;
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) offsets[E] = run;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kScanThreads) offsets[e] = s_off[e];
-  for (int e = warp; e < E; e += kScanThreads / 32)
-    for (int b = lane; b < B; b += 32) block_counts[static_cast<size_t>(b) * E + e] += s_off[e];
-}
-
-// Large T, pass 3: rows of every pair of the block.
+// Large T, pass 2: rows of every pair of the block.  Each block first derives
+// its own bases from the count matrix (every block reads all of it, B x E
+// ints): base[e] = offsets[e] + sum over blocks b' < b of counts[b'][e], with
+// offsets the exclusive scan of the expert totals; block 0 writes offsets.
 __global__ void __launch_bounds__(kTB)
     permute_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int k,
-                           const int32_t* __restrict__ block_base, int32_t* __restrict__ sorted_token,
-                           int32_t* __restrict__ inv_perm) {
+                           const int32_t* __restrict__ block_counts, int32_t* __restrict__ offsets,
+                           int32_t* __restrict__ sorted_token, int32_t* __restrict__ inv_perm) {
   __shared__ uint32_t mask[kMaxExperts * kMaskWords];
+  __shared__ int s_tot[kMaxExperts];
+  __shared__ int s_before[kMaxExperts];
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int tl = threadIdx.x, t = blockIdx.x * kTB + tl;
+  const int b = blockIdx.x, B = gridDim.x;
   for (int i = tl; i < E * kMaskWords; i += kTB) mask[i] = 0;
+  for (int e = tl; e < E; e += kTB) {
+    int before = 0, tot = 0;
+#pragma unroll 8
+    for (int bb = 0; bb < B; ++bb) {
+      const int c = block_counts[static_cast<size_t>(bb) * E + e];
+      tot += c;
+      if (bb < b) before += c;
+    }
+    s_tot[e] = tot;
+    s_before[e] = before;
+  }
   __syncthreads();
   // errors were recorded by the count pass
   const bool valid = t < T && mask_token(ids, t, tl, E, k, mask, nullptr);
-  __syncthreads();
+  const int total = block_exclusive_scan(s_tot, E);   // s_tot -> offsets
+  if (b == 0) {
+    for (int e = tl; e < E; e += kTB) offsets[e] = s_tot[e];
+    if (tl == 0) offsets[E] = total;
+  }
   if (t >= T) return;
-  const int32_t* base = block_base + static_cast<size_t>(blockIdx.x) * E;
   for (int j = 0; j < k; ++j) {
     if (valid) {
       const int e = ids[static_cast<size_t>(t) * k + j];
-      const int r = base[e] + mask_rank(mask, e, tl);
+      const int r = s_tot[e] + s_before[e] + mask_rank(mask, e, tl);
       sorted_token[r] = t;
       inv_perm[static_cast<size_t>(t) * k + j] = r;
     } else {
@@ -265,12 +234,10 @@ int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, 
     const int B = (T + kTB - 1) / kTB;
     if (launch_chained(permute_count_kernel, dim3(B), dim3(kTB), 0, stream, topk_ids, T, E, k, block_counts,
                        status) != cudaSuccess ||
-        launch_chained(permute_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, block_counts, B, E, offsets) !=
-            cudaSuccess ||
         launch_chained(permute_scatter_kernel, dim3(B), dim3(kTB), 0, stream, topk_ids, T, E, k,
-                       static_cast<const int32_t*>(block_counts), sorted_token, inv_perm) != cudaSuccess)
+                       static_cast<const int32_t*>(block_counts), offsets, sorted_token, inv_perm) != cudaSuccess)
       return MOE_ERR_CUDA;
-    *launches += 3;
+    *launches += 2;
   }
   if (x_perm) {
     long long grid = (static_cast<long long>(T) + 7) / 8;

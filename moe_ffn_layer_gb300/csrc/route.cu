@@ -184,31 +184,47 @@ __device__ __forceinline__ float warp_dot_fp32(const __nv_bfloat16* x, const flo
 
 // k rounds of arg-max over v (lane-strided, E entries); returns this lane's
 // round winner (lane r keeps round r) and the value of round `extra` (-inf if none).
+// Order-preserving map of a float to a 32-bit key (a larger float gives a
+// larger key; -0 and +0 give the same key).  Key 0 is below every float's key
+// (the key of -inf is 0x007fffff) and marks "not a candidate".
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// `rounds` rounds of "take the largest remaining logit, the smallest expert
+// id among equal values", one warp, lane j keeping round j's (id, value);
+// last_v = the value of the final round.  Each round is a lane-local pass over
+// the lane's NPL keys and two warp reductions (max key, then min id among
+// the lanes holding it).
 template <int NPL>
 __device__ __forceinline__ void warp_select(const float (&v)[NPL], int E, int rounds, int& my_id, float& my_v,
                                             float& last_v) {
   const int lane = threadIdx.x & 31;
-  uint32_t taken = 0;   // bit i: element i of this lane already chosen
+  uint32_t key[NPL];
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) key[i] = i * 32 + lane < E ? order_key(v[i]) : 0u;
   my_id = 0x7fffffff;
   my_v = -INFINITY;
   last_v = -INFINITY;
   for (int r = 0; r < rounds; ++r) {
-    float best = -INFINITY;
-    int bid = 0x7fffffff;
+    uint32_t bk = 0;
+    int bi = 0;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      const int e = i * 32 + lane;
-      if (e < E && !(taken >> i & 1u) && (v[i] > best || (v[i] == best && e < bid))) { best = v[i]; bid = e; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (ob > best || (ob == best && oi < bid)) { best = ob; bid = oi; }
-    }
+    for (int i = 0; i < NPL; ++i)
+      if (key[i] > bk) { bk = key[i]; bi = i; }   // strict: equal keys keep the smaller id
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const int bid = __reduce_min_sync(0xffffffffu, bk == m ? bi * 32 + lane : 0x7fffffff);
+    const float best = key_value(m);
     if (lane == r) { my_id = bid; my_v = best; }
     last_v = best;
-    if (bid < E && (bid & 31) == lane) taken |= 1u << (bid >> 5);
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (i * 32 + lane == bid) key[i] = 0u;
   }
 }
 
