@@ -424,6 +424,48 @@ def test_forward_batches_of_different_sizes_share_one_workspace():
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), T
 
 
+@pytest.mark.parametrize("T,H,E,k", [(700, 512, 8, 2), (100, 256, 2, 2)])
+def test_forward_matches_standalone_calls(T, H, E, k):
+    """At sizes where both matmuls take the tokens-on-M form (no split-K), the
+    layer output has the same bits as the standalone calls (route, permute,
+    both matmuls, shared expert, combine), and matches the oracle.  T = 100
+    takes the one-block sort."""
+    wl = synth.Workload("standalone", T, H, E, k, 256, 128, sigma_router=0.1, sigma_w=0.03)
+    inp = synth.make_inputs(wl, 23)
+    ref = om.forward(inp, wl.k)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    x = bf16_tensor(inp["x"], "cuda")
+    out = L.forward(x).clone()
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], f"forward T={T}")
+    wr, bias, wgu, wd, sgu, sd = L.tensors
+    rows = T * k
+    dev = "cuda"
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    tw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    rb, pb = B.moe_route_workspace_bytes(T, H, E), B.moe_permute_workspace_bytes(T, E)
+    rws = torch.empty(max(rb, 256), dtype=torch.uint8, device=dev)
+    pws = torch.empty(max(pb, 256), dtype=torch.uint8, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    st = torch.empty(rows, dtype=torch.int32, device=dev)
+    inv = torch.empty(rows, dtype=torch.int32, device=dev)
+    xp = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((rows, wl.I), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+    hs = torch.empty((T, wl.Is), dtype=torch.bfloat16, device=dev)
+    sh = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    out2 = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    B.moe_route(x, wr, bias, T, H, E, k, ids, tw, rws, rb, stream())
+    B.moe_permute(ids, x, T, H, E, k, offs, st, inv, xp, pws, pb, stream())
+    B.moe_grouped_gemm(xp, wgu, offs, E, rows, wl.I, H, 1, h, None, 0, stream())
+    B.moe_grouped_gemm(h, wd, offs, E, rows, H, wl.I, 0, y, None, 0, stream())
+    B.moe_grouped_gemm(x, sgu, None, 1, T, wl.Is, H, 1, hs, None, 0, stream())
+    B.moe_grouped_gemm(hs, sd, None, 1, T, H, wl.Is, 0, sh, None, 0, stream())
+    B.moe_unpermute_combine(y, inv, tw, sh, T, H, k, out2, stream())
+    no_device_error()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
 def test_forward_repeatable_and_launch_count():
     """Two calls give identical bits; the launch count is what the call reports."""
     L = layer("tiny", 16)
