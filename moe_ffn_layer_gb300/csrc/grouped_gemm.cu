@@ -53,9 +53,15 @@ constexpr int tmem_cols_pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 
 
 // SWAP = 0: tokens on M, W = BN (weight rows per unit).
 // SWAP = 1: weights on M, W = NMAX (token rows per unit).
-template <int SWAP, int W, int ACT>
+// Tokens-on-M pairs: CTAs run in clusters of two that share one operand tile,
+// each loading half of it with a multicast to both.
+//  MC = 1: the two 128-row halves of a 256-row unit with the same weight block;
+//          each CTA loads its own token rows and half of the weight block.
+//  MC = 2: one 128-row token tile against two adjacent weight blocks; each CTA
+//          loads its own weight block and 64 of the token rows.
+template <int SWAP, int W, int ACT, int MC = 0>
 struct Cfg {
-  static constexpr int kUnitRows = SWAP ? W : 128;                          // token rows per unit
+  static constexpr int kUnitRows = SWAP ? W : (MC == 1 ? 256 : 128);        // token rows per unit
   static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;
   static constexpr int kBBytes = W * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -167,11 +173,14 @@ struct WorkIter {
 // last arriver's sum), in K blocks; measured on decode shapes.
 constexpr int kPieceCost = 6;
 
-template <int SWAP, int W, int ACT>
+template <int SWAP, int W, int ACT, int MC = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_wgt,
                         const GemmArgs args) {
-  using C = Cfg<SWAP, W, ACT>;
+  static_assert(!MC || (!SWAP && W == 256 && (ACT == 0 || ACT == 1)), "pairs: tokens-on-M, 256-wide blocks");
+  constexpr int kTokHalf = 64 * kBK * 2;   // bytes of 64 token rows of a K block
+  using C = Cfg<SWAP, W, ACT, MC>;
+  constexpr uint16_t kPairMask = 0x3;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
@@ -193,11 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = args.G;
   const int NB = args.N / C::kOutCols;   // weight blocks per group
+  const int NBU = MC == 2 ? NB / 2 : NB;   // units per token tile
 
   // ---- prologue (may overlap the previous kernel of the stream): barriers,
   // tensor-map prefetch; then wait for that kernel's writes
   if (warp == 1 && lane == 0) {
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    // with pairs a stage is free once both CTAs' MMAs are done with it (the
+    // peer's multicast writes into this CTA's copy too)
+    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], MC ? 2 : 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
     mbar_init(done_bar, 1);
     fence_barrier_init();
@@ -205,6 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_tok);
     tma_prefetch_desc(&tm_wgt);
   }
+  // pairs: both CTAs' barriers exist before either multicasts into the other
+  if (MC) cluster_sync_all();
+  const int crank = MC ? static_cast<int>(cluster_ctarank()) : 0;
+  const int wgrid = MC ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);   // work lists
+  const int wcta = MC ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   chain_wait();
   const ChainReleaseAtExit release_next;
   // ---- group offsets into shared memory (all threads)
@@ -226,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rows = bad ? 0 : b - a;
         mx = max(mx, rows);
         s_ustart[g] = local;
-        local += ((rows + C::kUnitRows - 1) / C::kUnitRows) * NB;
+        local += ((rows + C::kUnitRows - 1) / C::kUnitRows) * NBU;
       }
     }
     int incl = local;
@@ -282,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = s_split[7];
   // a CTA without work (or every CTA, when the offsets failed their check)
   // leaves before it allocates tensor memory
-  if (units == 0 || WorkIter(mode, S, units, kblocks, gridDim.x, blockIdx.x).empty()) return;
+  if (units == 0 || WorkIter(mode, S, units, kblocks, wgrid, wcta).empty()) return;
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
@@ -307,6 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     wb = local / nrb;
     row0 = s_off[g] + rb * C::kUnitRows;
     nrows = min(rows - rb * C::kUnitRows, C::kUnitRows);
+    if (MC == 1) {   // this CTA's 128-row half (possibly empty: it still loads its weight half)
+      row0 += crank * 128;
+      nrows = max(0, min(nrows - crank * 128, 128));
+    }
+    if (MC == 2) wb = 2 * wb + crank;   // this CTA's weight block
   };
 
   const int wrows = ACT == 1 ? 2 * args.N : args.N;   // weight rows per group
@@ -320,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long issued = 0;
     int stage = 0;
     uint32_t phase = 0;
-    WorkIter wi(mode, S, units, kblocks, gridDim.x, blockIdx.x);
+    WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
     Piece pc;
     while (wi.next(pc)) {
       int g, row0, nrows, wb;
@@ -349,6 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (SWAP) {
             tma_load_2d(sa, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
             if (ACT == 1) tma_load_2d(sa + kTileRows128, &tm_wgt, &full_bar[stage], kc, wrow + args.N, pol_w);
+          } else if (MC == 1) {
+            // this CTA's half of the weight block, to both CTAs: the gate (rank 0) or
+            // up (rank 1) rows with SiLU*mul, else the first or second 128 rows
+            const int brow = ACT == 1 ? wrow + crank * args.N : wrow + crank * 128;
+            tma_load_2d_mc(sb + crank * kTileRows128, &tm_wgt, &full_bar[stage], kc, brow, kPairMask, pol_w);
           } else {
             if (ACT == 1) {
               tma_load_2d(sb, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
@@ -364,6 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (SWAP) {
             for (int j = 0; j < n16; ++j)
               tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &full_bar[stage], kc, row0 + 16 * j, pol_tok);
+          } else if (MC == 2) {
+            // this CTA's 64 of the tile's token rows, to both CTAs
+            tma_load_2d_mc(stok + crank * kTokHalf, &tm_tok, &full_bar[stage], kc, row0 + crank * 64, kPairMask,
+                           pol_tok);
           } else {
             const int kca = args.a_kblocks ? (kb % args.a_kblocks) * kBK : kc;
             tma_load_2d(stok, &tm_tok, &full_bar[stage], kca, row0, pol_tok);
@@ -388,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      WorkIter wi(mode, S, units, kblocks, gridDim.x, blockIdx.x);
+      WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
       Piece pc;
       for (; wi.next(pc); ++it) {
         const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
@@ -433,7 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_bf16(d_tmem, da + ka, db + ka, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
             }
           }
-          umma_commit(&empty_bar[stage]);      // frees the smem stage when these MMAs finish
+          // frees the smem stage when these MMAs finish (in both CTAs of a pair)
+          if (MC)
+            umma_commit_mc(&empty_bar[stage], kPairMask);
+          else
+            umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -448,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                    // TMEM lane quadrant of this warp
     const int lrow = q * 32 + lane;            // TMEM lane = accumulator row
     int it = 0;
-    WorkIter wi(mode, S, units, kblocks, gridDim.x, blockIdx.x);
+    WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
     Piece pc;
     for (; wi.next(pc); ++it) {
       const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
@@ -648,6 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  // pairs: neither CTA leaves while the other may still arrive on its barriers
+  if (MC) cluster_sync_all();
 }
 
 // ---------------------------------------------------------------- host side
@@ -713,24 +750,44 @@ SplitPlan split_plan(int G, int rows_max, int N, int act, int max_slots = kMaxSl
   return p;
 }
 
-template <int SWAP, int W, int ACT>
+template <int SWAP, int W, int ACT, int MC = 0>
 int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K, void* out,
                int* status, const GemmScratch* scratch, int grid_cap, cudaStream_t stream, int* launches,
                int max_slots = kMaxSlots, int K_a = 0, const int32_t* a_rows = nullptr, int a_src_rows = 0) {
-  using C = Cfg<SWAP, W, ACT>;
+  using C = Cfg<SWAP, W, ACT, MC>;
+  auto kernel = grouped_gemm_kernel<SWAP, W, ACT, MC>;
   static bool attr_done[64] = {};
+  static int max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !attr_done[dev]) {
-    if (cudaFuncSetAttribute(grouped_gemm_kernel<SWAP, W, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (dev < 64) attr_done[dev] = true;
+    int clusters = 0;
+    if (MC) {
+      // pairs of CTAs fit only where two SMs of one GPC are free: ask how many
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(2 * grid_cap);
+      q.blockDim = dim3(kThreads);
+      q.dynamicSmemBytes = C::kSmemBytes;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      q.attrs = at;
+      q.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &q) != cudaSuccess || clusters < 1) return MOE_ERR_CUDA;
+    }
+    if (dev < 64) {
+      max_clusters[dev] = clusters;
+      attr_done[dev] = true;
+    }
   }
   CUtensorMap tt, tw;
   const int wrows = ACT == 1 ? 2 * N : N;
-  const uint32_t tok_box = SWAP ? 16 : 128;
-  const uint32_t wgt_box = SWAP ? 128 : (ACT == 1 ? W / 2 : W);
+  const uint32_t tok_box = SWAP ? 16 : (MC == 2 ? 64 : 128);
+  const uint32_t wgt_box = SWAP ? 128 : (ACT == 1 || MC == 1 ? W / 2 : W);
   if (a_rows) {   // rows fetched one at a time by gather4: a one-row box over the source rows
     if (!make_map(&tt, a, static_cast<uint64_t>(a_src_rows), static_cast<uint64_t>(K), 1)) return MOE_ERR_CUDA;
   } else if (!make_map(&tt, a, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K_a ? K_a : K), tok_box)) {
@@ -739,8 +796,8 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   if (!make_map(&tw, w, static_cast<uint64_t>(G) * wrows, static_cast<uint64_t>(K), wgt_box)) return MOE_ERR_CUDA;
   // upper bound on the unit count: every non-empty group adds at most one partial row block
   const long long nonempty = offsets ? (G < rows_max ? G : rows_max) : 1;
-  long long bound =
-      (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) * (N / C::kOutCols);
+  long long bound = (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) *
+                    (N / C::kOutCols / (MC == 2 ? 2 : 1));
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
                 nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows};
   if (SWAP && scratch && scratch->counters && scratch->partials) {
@@ -753,14 +810,31 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
       bound *= kMaxSplit;
     }
   }
+  if (MC) {
+    // one work list per pair: at most grid_cap / 2 pairs, and no more than fit at once
+    long long pairs = grid_cap / 2;
+    const int mc = dev < 64 ? max_clusters[dev] : 1;
+    if (pairs > mc) pairs = mc;
+    if (pairs > bound) pairs = bound;
+    if (pairs < 1) pairs = 1;
+    if (launch_chained_cluster(kernel, dim3(static_cast<int>(2 * pairs)), dim3(kThreads), C::kSmemBytes, stream, 2,
+                               tt, tw, args) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    ++*launches;
+    return MOE_OK;
+  }
   int grid = static_cast<int>(bound < grid_cap ? bound : grid_cap);
   if (grid < 1) grid = 1;
-  if (launch_chained(grouped_gemm_kernel<SWAP, W, ACT>, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, tt, tw,
-                     args) != cudaSuccess)
+  if (launch_chained(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, tt, tw, args) != cudaSuccess)
     return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
 }
+
+// Tokens-on-M launches with 256-wide weight blocks run as multicast pairs:
+// one large group (no offsets) shares weight blocks (MC 1); several groups
+// share token tiles (MC 2), which wastes no rows at the groups' ragged ends.
+constexpr bool kPairs = true;
 
 }  // namespace
 
@@ -807,12 +881,24 @@ int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, in
                                        launches, max_slots, 0, a_rows, a_src_rows);
   }
   if (act == 1) {
+    if (N % 128 == 0 && kPairs && !a_rows && grid_cap >= 2 && !offsets)
+      return launch_cfg<0, 256, 1, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
+                                      launches);
+    if (N % 256 == 0 && kPairs && !a_rows && grid_cap >= 2)
+      return launch_cfg<0, 256, 1, 2>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
+                                      launches);
     if (N % 128 == 0)
       return launch_cfg<0, 256, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
                                    launches, kMaxSlots, 0, a_rows, a_src_rows);
     return launch_cfg<0, 128, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream, launches,
                                  kMaxSlots, 0, a_rows, a_src_rows);
   }
+  if (N % 256 == 0 && kPairs && !a_rows && grid_cap >= 2 && !offsets)
+    return launch_cfg<0, 256, 0, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
+                                    launches);
+  if (N % 512 == 0 && kPairs && !a_rows && grid_cap >= 2)
+    return launch_cfg<0, 256, 0, 2>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
+                                    launches);
   if (N % 256 == 0)
     return launch_cfg<0, 256, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream, launches,
                                  kMaxSlots, 0, a_rows, a_src_rows);
