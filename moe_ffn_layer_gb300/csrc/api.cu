@@ -280,16 +280,29 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
   const int rows = T * d->k;
   int n = 0;
 
+  // SMs for the two streams.  At decode sizes both are weight streams that
+  // run side by side for the whole call: the shared expert gets the SMs in
+  // proportion to its share of the weight bytes (at least 8, at most half),
+  // the routed matmuls the rest.  Larger batches give both streams every SM.
+  int side_sms = di->sms, main_sms = di->sms;
+  if (T <= moe::route_small_max_tokens() && has_shared) {
+    const double shared_bytes = 3.0 * d->I_s * d->H * 2;
+    const double routed_bytes = 3.0 * d->I * d->H * 2 * std::min<long long>(d->E, static_cast<long long>(T) * d->k);
+    int c = static_cast<int>(di->sms * shared_bytes / (shared_bytes + routed_bytes) + 0.5);
+    c = std::max(8, std::min(c, di->sms / 2));
+    side_sms = c;
+    main_sms = di->sms - c;
+  }
   // shared expert on the side stream, forked from `stream`
   auto fork_shared = [&]() -> int {
     if (!has_shared) return MOE_OK;
     if (cudaEventRecord(ev_fork, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamWaitEvent(side, ev_fork, 0) != cudaSuccess) return MOE_ERR_CUDA;
     int r = moe::grouped_gemm_launch(x, w->ws_gate_up, nullptr, 1, T, d->I_s, d->H, 1, hs, di->status, &gside,
-                                     di->sms, side, &n);
+                                     side_sms, side, &n);
     if (!r)
       r = moe::grouped_gemm_launch(hs, w->ws_down, nullptr, 1, T, d->H, d->I_s, 0, s, di->status, &gside,
-                                   di->sms, side, &n);
+                                   side_sms, side, &n);
     if (r) return r;
     return cudaEventRecord(ev_join, side) != cudaSuccess ? MOE_ERR_CUDA : MOE_OK;
   };
@@ -322,12 +335,12 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
     // cannot feed full 128-row tiles
     rc = T <= moe::route_small_max_tokens()
              ? moe::grouped_gemm_launch(x, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, &gmain,
-                                        di->sms, stream, &n, sorted, T)
+                                        main_sms, stream, &n, sorted, T)
              : moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status,
                                         &gmain, di->sms, stream, &n);
   if (!rc)
     rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, &gmain,
-                                  di->sms, stream, &n);
+                                  main_sms, stream, &n);
   if (rc) return rc;
   // join, then combine
   if (has_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
