@@ -53,15 +53,15 @@ constexpr int tmem_cols_pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 
 
 // SWAP = 0: tokens on M, W = BN (weight rows per unit).
 // SWAP = 1: weights on M, W = NMAX (token rows per unit).
-// Tokens-on-M pairs: CTAs run in clusters of two that share one operand tile,
-// each loading half of it with a multicast to both.
-//  MC = 1: the two 128-row halves of a 256-row unit with the same weight block;
-//          each CTA loads its own token rows and half of the weight block.
-//  MC = 2: one 128-row token tile against two adjacent weight blocks; each CTA
-//          loads its own weight block and 64 of the token rows.
+// MC = 1 (tokens-on-M, 256-wide weight blocks): CTAs run in clusters of two
+// that share one operand tile, each loading half of it with a multicast to
+// both.  A group's 128-row tiles go in twos: the two tiles of a pair share the
+// weight block (each CTA loads its own token rows and half of the weights);
+// an odd last tile is shared by two adjacent weight blocks instead (each CTA
+// loads its own weights and 64 of the tile's token rows).
 template <int SWAP, int W, int ACT, int MC = 0>
 struct Cfg {
-  static constexpr int kUnitRows = SWAP ? W : (MC == 1 ? 256 : 128);        // token rows per unit
+  static constexpr int kUnitRows = SWAP ? W : 128;                          // token rows per unit
   static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;
   static constexpr int kBBytes = W * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -202,7 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = args.G;
   const int NB = args.N / C::kOutCols;   // weight blocks per group
-  const int NBU = MC == 2 ? NB / 2 : NB;   // units per token tile
 
   // ---- prologue (may overlap the previous kernel of the stream): barriers,
   // tensor-map prefetch; then wait for that kernel's writes
@@ -243,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rows = bad ? 0 : b - a;
         mx = max(mx, rows);
         s_ustart[g] = local;
-        local += ((rows + C::kUnitRows - 1) / C::kUnitRows) * NBU;
+        // pairs: (tiles / 2) weight-sharing units per block, + NB / 2 token-sharing ones for an odd tile
+        local += ((rows + C::kUnitRows - 1) / C::kUnitRows) * (MC ? NB / 2 : NB);
       }
     }
     int incl = local;
@@ -309,8 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // unit index -> group g, first token row, token rows in the unit, weight block
-  auto decode = [&](int idx, int& g, int& row0, int& nrows, int& wb) {
+  // unit index -> group g, this CTA's first token row, token rows, weight block;
+  // kind (pairs): 0 = the pair shares the weight block, 1 = the token tile
+  auto decode = [&](int idx, int& g, int& row0, int& nrows, int& wb, int& kind) {
     int lo = 0, hi = G - 1;
     while (lo < hi) {                      // last g with ustart[g] <= idx
       const int mid = (lo + hi + 1) >> 1;
@@ -320,15 +321,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows = s_off[g + 1] - s_off[g];
     const int nrb = (rows + C::kUnitRows - 1) / C::kUnitRows;
     const int local = idx - s_ustart[g];
+    kind = 0;
+    if (MC) {
+      const int np = nrb / 2;              // tile pairs
+      if (local < np * NB) {               // tiles 2rb and 2rb+1, one weight block
+        const int rb = local % np;
+        wb = local / np;
+        row0 = s_off[g] + (2 * rb + crank) * 128;
+        nrows = min(rows - (2 * rb + crank) * 128, 128);
+      } else {                             // the odd last tile, weight blocks 2j and 2j+1
+        kind = 1;
+        wb = 2 * (local - np * NB) + crank;
+        row0 = s_off[g] + (nrb - 1) * 128;
+        nrows = rows - (nrb - 1) * 128;
+      }
+      return;
+    }
     const int rb = local % nrb;
     wb = local / nrb;
     row0 = s_off[g] + rb * C::kUnitRows;
     nrows = min(rows - rb * C::kUnitRows, C::kUnitRows);
-    if (MC == 1) {   // this CTA's 128-row half (possibly empty: it still loads its weight half)
-      row0 += crank * 128;
-      nrows = max(0, min(nrows - crank * 128, 128));
-    }
-    if (MC == 2) wb = 2 * wb + crank;   // this CTA's weight block
   };
 
   const int wrows = ACT == 1 ? 2 * args.N : args.N;   // weight rows per group
@@ -345,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
     Piece pc;
     while (wi.next(pc)) {
-      int g, row0, nrows, wb;
-      decode(pc.u, g, row0, nrows, wb);
+      int g, row0, nrows, wb, kind;
+      decode(pc.u, g, row0, nrows, wb, kind);
       const int wrow = g * wrows + wb * C::kOutCols;
       const int n16 = (nrows + 15) >> 4;
       // token rows fetched: SWAP 16-row multiples; tokens-on-M all 128 rows
@@ -371,11 +383,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (SWAP) {
             tma_load_2d(sa, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
             if (ACT == 1) tma_load_2d(sa + kTileRows128, &tm_wgt, &full_bar[stage], kc, wrow + args.N, pol_w);
-          } else if (MC == 1) {
-            // this CTA's half of the weight block, to both CTAs: the gate (rank 0) or
-            // up (rank 1) rows with SiLU*mul, else the first or second 128 rows
-            const int brow = ACT == 1 ? wrow + crank * args.N : wrow + crank * 128;
-            tma_load_2d_mc(sb + crank * kTileRows128, &tm_wgt, &full_bar[stage], kc, brow, kPairMask, pol_w);
+          } else if (MC) {
+            // weight rows in two 128-row halves: gate | up with SiLU*mul, else rows
+            // 0..127 | 128..255 of the block; a weight-sharing pair loads one half
+            // per CTA, to both
+            const int second = ACT == 1 ? args.N : 128;
+            if (kind == 0) {
+              tma_load_2d_mc(sb + crank * kTileRows128, &tm_wgt, &full_bar[stage], kc, wrow + crank * second,
+                             kPairMask, pol_w);
+            } else {
+              tma_load_2d(sb, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
+              tma_load_2d(sb + kTileRows128, &tm_wgt, &full_bar[stage], kc, wrow + second, pol_w);
+            }
           } else {
             if (ACT == 1) {
               tma_load_2d(sb, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
@@ -391,10 +410,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (SWAP) {
             for (int j = 0; j < n16; ++j)
               tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &full_bar[stage], kc, row0 + 16 * j, pol_tok);
-          } else if (MC == 2) {
-            // this CTA's 64 of the tile's token rows, to both CTAs
-            tma_load_2d_mc(stok + crank * kTokHalf, &tm_tok, &full_bar[stage], kc, row0 + crank * 64, kPairMask,
-                           pol_tok);
+          } else if (MC) {
+            // token rows in two 64-row halves; a token-sharing pair loads one half
+            // per CTA, to both
+            if (kind == 0) {
+              tma_load_2d(stok, &tm_tok, &full_bar[stage], kc, row0, pol_tok);
+              tma_load_2d(stok + kTokHalf, &tm_tok, &full_bar[stage], kc, row0 + 64, pol_tok);
+            } else {
+              tma_load_2d_mc(stok + crank * kTokHalf, &tm_tok, &full_bar[stage], kc, row0 + crank * 64, kPairMask,
+                             pol_tok);
+            }
           } else {
             const int kca = args.a_kblocks ? (kb % args.a_kblocks) * kBK : kc;
             tma_load_2d(stok, &tm_tok, &full_bar[stage], kca, row0, pol_tok);
@@ -427,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t idesc;
         int chains = 1, cw = 0;
         if (SWAP) {
-          int g, row0, nrows, wb;
-          decode(pc.u, g, row0, nrows, wb);
+          int g, row0, nrows, wb, kind;
+          decode(pc.u, g, row0, nrows, wb, kind);
           const int n16 = (nrows + 15) >> 4;
           idesc = idesc_bf16_f32(128, n16 * 16);
           chains = swap_chains(n16, C::kAccCols, ACT == 1);
@@ -489,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
       const uint32_t aphase = (C::kNumAcc == 2 ? (it >> 1) : it) & 1;
       const int u = pc.u;
-      int g, row0, nrows, wb;
-      decode(u, g, row0, nrows, wb);
+      int g, row0, nrows, wb, kind;
+      decode(u, g, row0, nrows, wb, kind);
       bool ok = mbar_wait(&tfull_bar[ab], aphase, abort_flag, args.status);
       if (P > 1) {
         // the split path meets at named barriers: the four warps leave together or not at all
@@ -786,8 +811,8 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   }
   CUtensorMap tt, tw;
   const int wrows = ACT == 1 ? 2 * N : N;
-  const uint32_t tok_box = SWAP ? 16 : (MC == 2 ? 64 : 128);
-  const uint32_t wgt_box = SWAP ? 128 : (ACT == 1 || MC == 1 ? W / 2 : W);
+  const uint32_t tok_box = SWAP ? 16 : (MC ? 64 : 128);
+  const uint32_t wgt_box = SWAP ? 128 : (ACT == 1 || MC ? W / 2 : W);
   if (a_rows) {   // rows fetched one at a time by gather4: a one-row box over the source rows
     if (!make_map(&tt, a, static_cast<uint64_t>(a_src_rows), static_cast<uint64_t>(K), 1)) return MOE_ERR_CUDA;
   } else if (!make_map(&tt, a, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K_a ? K_a : K), tok_box)) {
@@ -797,7 +822,7 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   // upper bound on the unit count: every non-empty group adds at most one partial row block
   const long long nonempty = offsets ? (G < rows_max ? G : rows_max) : 1;
   long long bound = (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) *
-                    (N / C::kOutCols / (MC == 2 ? 2 : 1));
+                    (N / C::kOutCols / (MC ? 2 : 1));
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
                 nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows};
   if (SWAP && scratch && scratch->counters && scratch->partials) {
@@ -831,9 +856,8 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   return MOE_OK;
 }
 
-// Tokens-on-M launches with 256-wide weight blocks run as multicast pairs:
-// one large group (no offsets) shares weight blocks (MC 1); several groups
-// share token tiles (MC 2), which wastes no rows at the groups' ragged ends.
+// Tokens-on-M launches with an even number of 256-wide weight blocks run as
+// multicast pairs.
 constexpr bool kPairs = true;
 
 }  // namespace
@@ -881,11 +905,8 @@ int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, in
                                        launches, max_slots, 0, a_rows, a_src_rows);
   }
   if (act == 1) {
-    if (N % 128 == 0 && kPairs && !a_rows && grid_cap >= 2 && !offsets)
-      return launch_cfg<0, 256, 1, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
-                                      launches);
     if (N % 256 == 0 && kPairs && !a_rows && grid_cap >= 2)
-      return launch_cfg<0, 256, 1, 2>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
+      return launch_cfg<0, 256, 1, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
                                       launches);
     if (N % 128 == 0)
       return launch_cfg<0, 256, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
@@ -893,11 +914,8 @@ int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, in
     return launch_cfg<0, 128, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream, launches,
                                  kMaxSlots, 0, a_rows, a_src_rows);
   }
-  if (N % 256 == 0 && kPairs && !a_rows && grid_cap >= 2 && !offsets)
-    return launch_cfg<0, 256, 0, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
-                                    launches);
   if (N % 512 == 0 && kPairs && !a_rows && grid_cap >= 2)
-    return launch_cfg<0, 256, 0, 2>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
+    return launch_cfg<0, 256, 0, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,
                                     launches);
   if (N % 256 == 0)
     return launch_cfg<0, 256, 0>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream, launches,
