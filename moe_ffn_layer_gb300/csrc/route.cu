@@ -36,41 +36,58 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
-// fp32 SIMT GEMM: logits[T][E] = x[T][H] . Wr[E][H]^T.  CTA tile 64 x 64,
-// K chunk 32, 256 threads each owning a 4 x 4 block of outputs.
+// fp32 SIMT GEMM over one slice of H: part[z][T][E] = x[T][hz] . Wr[E][hz]^T
+// for the z-th of gridDim.z equal slices hz of H (one slice: the logits).  CTA
+// tile 64 x 64, K chunk 32, 256 threads each owning a 4 x 4 block of outputs;
+// the next chunk is loaded into registers while the current one is used.
 constexpr int kRT = 64, kRE = 64, kRK = 32;
 
 __global__ void __launch_bounds__(256)
     router_tile_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, int T, int H, int E,
-                       float* __restrict__ logits) {
+                       float* __restrict__ part) {
   __shared__ float xs[kRK][kRT + 4];
   __shared__ float ws[kRK][kRE + 4];
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE;
+  const int HS = H / gridDim.z;
+  const int kbeg = blockIdx.z * HS, kend = kbeg + HS;
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;   // 16 x 16 threads
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < H; k0 += kRK) {
-    {  // x tile: 64 rows x 32 bf16 = 256 x uint4 (8 bf16 each)
-      const int r = tid >> 2, c = (tid & 3) * 8;
-      float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (t0 + r < T && k0 + c < H) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + r) * H + k0 + c));
-        bf16x8_to_f32(v, f);
-      }
+  // this thread's share of a chunk: 8 bf16 of one x row, 2 x 4 fp32 of Wr rows
+  const int xr = tid >> 2, xc = (tid & 3) * 8;
+  uint4 xv;
+  float4 wv[2];
+  auto fetch = [&](int k0) {
+    xv = make_uint4(0, 0, 0, 0);
+    if (t0 + xr < T && k0 + xc < kend)
+      xv = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + xr) * H + k0 + xc));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) xs[c + i][r] = f[i];
-    }
-#pragma unroll
-    for (int p = 0; p < 2; ++p) {  // Wr tile: 64 rows x 32 fp32 = 512 x float4
+    for (int p = 0; p < 2; ++p) {
       const int idx = tid + p * 256;
       const int r = idx >> 3, c = (idx & 7) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e0 + r < E && k0 + c < H) v = __ldg(reinterpret_cast<const float4*>(wr + static_cast<size_t>(e0 + r) * H + k0 + c));
-      ws[c + 0][r] = v.x; ws[c + 1][r] = v.y; ws[c + 2][r] = v.z; ws[c + 3][r] = v.w;
+      wv[p] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e0 + r < E && k0 + c < kend)
+        wv[p] = __ldg(reinterpret_cast<const float4*>(wr + static_cast<size_t>(e0 + r) * H + k0 + c));
+    }
+  };
+  float acc[4][4] = {};
+  fetch(kbeg);
+  for (int k0 = kbeg; k0 < kend; k0 += kRK) {
+    {
+      float f[8];
+      bf16x8_to_f32(xv, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[xc + i][xr] = f[i];
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int idx = tid + p * 256;
+        const int r = idx >> 3, c = (idx & 7) * 4;
+        ws[c + 0][r] = wv[p].x; ws[c + 1][r] = wv[p].y; ws[c + 2][r] = wv[p].z; ws[c + 3][r] = wv[p].w;
+      }
     }
     __syncthreads();
+    if (k0 + kRK < kend) fetch(k0 + kRK);
 #pragma unroll 8
     for (int kk = 0; kk < kRK; ++kk) {
       float a[4], b[4];
@@ -83,6 +100,7 @@ __global__ void __launch_bounds__(256)
     }
     __syncthreads();
   }
+  float* out = part + static_cast<size_t>(blockIdx.z) * T * E;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int t = t0 + ty * 4 + i;
@@ -90,56 +108,87 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + tx * 4 + j;
-      if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j];
+      if (e < E) out[static_cast<size_t>(t) * E + e] = acc[i][j];
     }
   }
 }
 
-// 16 < T < 512: one warp per (expert, chunk of 16 tokens); lanes stride H
-// eight elements at a time (16-byte loads, all independent), each lane keeps
-// 16 fp32 partial sums, then a fixed butterfly adds the lanes.  Wr rows are
-// read once per chunk (from L2 after the first).
-constexpr int kChunkT = 16;
+// H slices for the tiled router: enough CTAs to cover the GPU, at most
+// kMaxSlices, each slice a whole number of K chunks.
+int tile_slices(int T, int H, int E, int sms) {
+  const int tiles = ((T + kRT - 1) / kRT) * ((E + kRE - 1) / kRE);
+  int S = 1;
+  while (S < 8 && tiles * S * 2 <= sms && H % (2 * S * kRK) == 0) S *= 2;
+  return S;
+}
 
+constexpr int kSliceH = 512;            // H elements per partial-logit warp
+constexpr int kMaxSlices = 8;           // at most this many H slices
+constexpr int kChunkT = 16;             // token rows per partial-logit warp
+
+int small_slices(int H) {
+  int S = H / kSliceH;
+  if (S < 1) S = 1;
+  if (S > kMaxSlices) S = kMaxSlices;
+  while (S > 1 && H % (S * 8)) --S;
+  return S;
+}
+
+// One warp: acc[t] = sum over h in [h_begin, h_end) of x[t, h] * w[h] for the
+// NT token rows of x (rows at or past nrows re-read row nrows-1, so that every
+// load of a step is issued unconditionally); lanes stride h eight elements at
+// a time (16-byte loads), then the lanes' sums are added across the warp.
+template <int NT>
+__device__ __forceinline__ void warp_partial_dot(const __nv_bfloat16* __restrict__ x, int H, int nrows,
+                                                 const float* __restrict__ w, int h_begin, int h_end,
+                                                 float (&acc)[NT]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+#pragma unroll 2
+  for (int h0 = h_begin + lane * 8; h0 < h_end; h0 += 256) {
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + h0));
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + h0 + 4));
+    uint4 xv[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+      xv[t] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t < nrows ? t : nrows - 1) * H + h0));
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float f[8];
+      bf16x8_to_f32(xv[t], f);
+      float v = acc[t];
+      v = fmaf(f[0], w0.x, v); v = fmaf(f[1], w0.y, v); v = fmaf(f[2], w0.z, v); v = fmaf(f[3], w0.w, v);
+      v = fmaf(f[4], w1.x, v); v = fmaf(f[5], w1.y, v); v = fmaf(f[6], w1.z, v); v = fmaf(f[7], w1.w, v);
+      acc[t] = v;
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+  }
+}
+
+// 16 < T < 512: partial logits part[s][t][e] over slice s of H, one warp per
+// (expert, slice, 16-token chunk); the top-k kernel adds the slices.
 __global__ void __launch_bounds__(256)
-    router_gemv_chunk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, int T, int H, int E,
-                             float* __restrict__ logits) {
+    router_chunk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wr, int T, int H, int E,
+                        int S, float* __restrict__ part) {
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int e = gw % E, t0 = (gw / E) * kChunkT;
+  const int e = gw % E, sl = (gw / E) % S, t0 = (gw / E / S) * kChunkT;
   if (t0 >= T) return;
   const int nt = min(kChunkT, T - t0);
+  const int HS = H / S;
   float acc[kChunkT];
+  warp_partial_dot<kChunkT>(x + static_cast<size_t>(t0) * H, H, nt, wr + static_cast<size_t>(e) * H, sl * HS,
+                            (sl + 1) * HS, acc);
 #pragma unroll
-  for (int t = 0; t < kChunkT; ++t) acc[t] = 0.f;
-  const float* w = wr + static_cast<size_t>(e) * H;
-  const __nv_bfloat16* xc = x + static_cast<size_t>(t0) * H;
-#pragma unroll 2
-  for (int h0 = lane * 8; h0 < H; h0 += 256) {
-    const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + h0));
-    const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + h0 + 4));
-#pragma unroll
-    for (int t = 0; t < kChunkT; ++t) {
-      if (t < nt) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xc + static_cast<size_t>(t) * H + h0));
-        float f[8];
-        bf16x8_to_f32(xv, f);
-        float v = acc[t];
-        v = fmaf(f[0], w0.x, v); v = fmaf(f[1], w0.y, v); v = fmaf(f[2], w0.z, v); v = fmaf(f[3], w0.w, v);
-        v = fmaf(f[4], w1.x, v); v = fmaf(f[5], w1.y, v); v = fmaf(f[6], w1.z, v); v = fmaf(f[7], w1.w, v);
-        acc[t] = v;
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kChunkT; ++t) {
-    float v = acc[t];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == t && t < nt) logits[static_cast<size_t>(t0 + t) * E + e] = v;
-  }
+  for (int t = 0; t < kChunkT; ++t)
+    if (lane == t && t < nt) part[(static_cast<size_t>(sl) * T + t0 + t) * E + e] = acc[t];
 }
 
 // Top-k of one token by one warp: k rounds of a warp arg-max over the E
@@ -229,15 +278,36 @@ __device__ __forceinline__ void warp_select(const float (&v)[NPL], int E, int ro
 }
 
 // NPL = logits per lane (E <= 32 * NPL).
+// S > 1: the logits are S partial slices, slice s at l + s * stride, added in
+// slice order (every load issued before the first add).
 template <int NPL>
 __device__ void warp_topk_softmax(const float* l, const float* bias, int E, int k, int32_t* ids_out, float* w_out,
-                                  const Refine* refine = nullptr) {
+                                  const Refine* refine = nullptr, int S = 1, size_t stride = 0) {
   const int lane = threadIdx.x & 31;
   float v[NPL];
+  if (S == 1) {
 #pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = i * 32 + lane;
-    v[i] = e < E ? l[e] + (bias ? bias[e] : 0.f) : -INFINITY;
+    for (int i = 0; i < NPL; ++i) {
+      const int e = i * 32 + lane;
+      v[i] = e < E ? l[e] + (bias ? bias[e] : 0.f) : -INFINITY;
+    }
+  } else {
+    float p[NPL][kMaxSlices];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = min(i * 32 + lane, E - 1);
+#pragma unroll
+      for (int sl = 0; sl < kMaxSlices; ++sl) p[i][sl] = l[(sl < S ? sl : S - 1) * stride + e];
+    }
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = i * 32 + lane;
+      float acc = p[i][0];
+#pragma unroll
+      for (int sl = 1; sl < kMaxSlices; ++sl)
+        if (sl < S) acc += p[i][sl];
+      v[i] = e < E ? acc + (bias ? bias[e] : 0.f) : -INFINITY;
+    }
   }
   int my_id;
   float my_v, last_v;
@@ -278,18 +348,20 @@ __device__ void warp_topk_softmax(const float* l, const float* bias, int E, int 
 
 // refine_wr != nullptr: the logits came from the tensor cores; near ties are
 // re-evaluated in fp32 from x and Wr (see warp_topk_softmax).
+// S > 1: logits holds S partial slices [S][T][E], added in slice order.
 template <int NPL>
 __global__ void __launch_bounds__(256)
     topk_softmax_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
                         int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-                        const __nv_bfloat16* __restrict__ x, const float* __restrict__ refine_wr, int H) {
+                        const __nv_bfloat16* __restrict__ x, const float* __restrict__ refine_wr, int H, int S) {
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   const Refine r{x + static_cast<size_t>(t) * H, refine_wr, H};
   warp_topk_softmax<NPL>(logits + static_cast<size_t>(t) * E, bias, E, k, topk_ids + static_cast<size_t>(t) * k,
-                         topk_w + static_cast<size_t>(t) * k, refine_wr ? &r : nullptr);
+                         topk_w + static_cast<size_t>(t) * k, refine_wr ? &r : nullptr, S,
+                         static_cast<size_t>(T) * E);
 }
 
 // wr3[e][j*H + h] = j-th bf16 term of Wr[e][h] (j = 0 hi, 1 mid, 2 lo).
@@ -316,9 +388,7 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------- T <= 16: one kernel
 
 constexpr int kSmallT = 16;
-constexpr int kSliceH = 512;            // H elements per partial-logit warp
 constexpr int kSmallThreads = 256;
-constexpr int kMaxSlices = 8;           // at most this many H slices
 
 struct SmallArgs {
   const __nv_bfloat16* x;     // [T][H]
@@ -359,34 +429,10 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
     const int e = gw % E, sl = gw / E;
     const int HS = a.H / S;
     float acc[NT];
+    warp_partial_dot<NT>(a.x, a.H, T, a.wr + static_cast<size_t>(e) * a.H, sl * HS, (sl + 1) * HS, acc);
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-    const float* w = a.wr + static_cast<size_t>(e) * a.H;
-#pragma unroll 2
-    for (int h0 = sl * HS + lane * 8; h0 < (sl + 1) * HS; h0 += 256) {
-      const float4 w0 = __ldg(reinterpret_cast<const float4*>(w + h0));
-      const float4 w1 = __ldg(reinterpret_cast<const float4*>(w + h0 + 4));
-      uint4 xv[NT];
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        xv[t] = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t < T ? t : T - 1) * a.H + h0));
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        float f[8];
-        bf16x8_to_f32(xv[t], f);
-        float v = acc[t];
-        v = fmaf(f[0], w0.x, v); v = fmaf(f[1], w0.y, v); v = fmaf(f[2], w0.z, v); v = fmaf(f[3], w0.w, v);
-        v = fmaf(f[4], w1.x, v); v = fmaf(f[5], w1.y, v); v = fmaf(f[6], w1.z, v); v = fmaf(f[7], w1.w, v);
-        acc[t] = v;
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      float v = acc[t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == t && t < T) a.part[(static_cast<size_t>(sl) * T + t) * E + e] = v;
-    }
+    for (int t = 0; t < NT; ++t)
+      if (lane == t && t < T) a.part[(static_cast<size_t>(sl) * T + t) * E + e] = acc[t];
   }
   // the last CTA to finish its partials goes on
   __threadfence();
@@ -468,22 +514,19 @@ cudaError_t launch_small(int npl, int nt, int grid, cudaStream_t stream, const S
   return launch_small_nt<16>(nt, grid, stream, a);
 }
 
-int small_slices(int H) {
-  int S = H / kSliceH;
-  if (S < 1) S = 1;
-  if (S > kMaxSlices) S = kMaxSlices;
-  while (S > 1 && H % (S * 8)) --S;
-  return S;
-}
 
 }  // namespace
 
 constexpr int kTcMinT = 512;   // from this many tokens the logits come from the tensor cores
+constexpr int kTileMinT = 128; // from this many tokens (short of that) the tiled fp32 GEMM
 
 bool route_uses_tc(int T, int H, int E) { return T >= kTcMinT && E % 64 == 0 && H % 64 == 0; }
 
 size_t route_ws_bytes(int T, int H, int E) {
-  size_t b = align_up(static_cast<size_t>(T) * E * sizeof(float) * (T <= kSmallT ? small_slices(H) : 1));
+  // partial-logit slices: by H for the small and chunked routers, up to
+  // kMaxSlices for the tiled one, one for the tensor-core one
+  const int slices = T < kTileMinT ? small_slices(H) : (route_uses_tc(T, H, E) ? 1 : kMaxSlices);
+  size_t b = align_up(static_cast<size_t>(T) * E * sizeof(float) * slices);
   if (route_uses_tc(T, H, E)) b += align_up(static_cast<size_t>(E) * 3 * H * 2);
   return b;
 }
@@ -511,6 +554,7 @@ int route_launch(const void* x, const float* w_router, const float* bias, int T,
     ++*launches;
     return MOE_OK;
   }
+  int S = 1;   // partial-logit slices the top-k adds
   if (route_uses_tc(T, H, E)) {
     __nv_bfloat16* wr3 = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<uint8_t*>(logits_ws) +
                                                           align_up(static_cast<size_t>(T) * E * sizeof(float)));
@@ -521,14 +565,16 @@ int route_launch(const void* x, const float* w_router, const float* bias, int T,
     ++*launches;
     const int rc = router_gemm_launch(x, wr3, T, H, E, logits_ws, status, grid_cap, stream, launches);
     if (rc) return rc;
-  } else if (T < kTcMinT) {
-    const long long warps = static_cast<long long>(E) * ((T + kChunkT - 1) / kChunkT);
-    if (launch_chained(router_gemv_chunk_kernel, dim3(static_cast<int>((warps + 7) / 8)), dim3(256), 0, stream, xb,
-                       w_router, T, H, E, logits_ws) != cudaSuccess)
+  } else if (T < kTileMinT) {
+    S = small_slices(H);
+    const long long warps = static_cast<long long>(E) * S * ((T + kChunkT - 1) / kChunkT);
+    if (launch_chained(router_chunk_kernel, dim3(static_cast<int>((warps + 7) / 8)), dim3(256), 0, stream, xb,
+                       w_router, T, H, E, S, logits_ws) != cudaSuccess)
       return MOE_ERR_CUDA;
     ++*launches;
   } else {
-    dim3 grid((T + kRT - 1) / kRT, (E + kRE - 1) / kRE);
+    S = tile_slices(T, H, E, grid_cap);
+    dim3 grid((T + kRT - 1) / kRT, (E + kRE - 1) / kRE, S);
     if (launch_chained(router_tile_kernel, grid, dim3(256), 0, stream, xb, w_router, T, H, E, logits_ws) != cudaSuccess)
       return MOE_ERR_CUDA;
     ++*launches;
@@ -538,13 +584,13 @@ int route_launch(const void* x, const float* w_router, const float* bias, int T,
   cudaError_t rc;
   if (E <= 128)
     rc = launch_chained(topk_softmax_kernel<4>, dim3(tg), dim3(256), 0, stream, static_cast<const float*>(logits_ws),
-                        bias, T, E, k, topk_ids, topk_w, xb, rw, H);
+                        bias, T, E, k, topk_ids, topk_w, xb, rw, H, S);
   else if (E <= 256)
     rc = launch_chained(topk_softmax_kernel<8>, dim3(tg), dim3(256), 0, stream, static_cast<const float*>(logits_ws),
-                        bias, T, E, k, topk_ids, topk_w, xb, rw, H);
+                        bias, T, E, k, topk_ids, topk_w, xb, rw, H, S);
   else
     rc = launch_chained(topk_softmax_kernel<16>, dim3(tg), dim3(256), 0, stream, static_cast<const float*>(logits_ws),
-                        bias, T, E, k, topk_ids, topk_w, xb, rw, H);
+                        bias, T, E, k, topk_ids, topk_w, xb, rw, H, S);
   if (rc != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
