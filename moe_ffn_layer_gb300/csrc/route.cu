@@ -311,10 +311,13 @@ __device__ void warp_topk_softmax(const float* l, const float* bias, int E, int 
   }
   int my_id;
   float my_v, last_v;
+  bool selected = false;
   if (refine && k < E) {
     warp_select(v, E, k + 1, my_id, my_v, last_v);   // round k holds the (k+1)-th value
     const float vk = __shfl_sync(0xffffffffu, my_v, k - 1);
-    if (vk - last_v < kRefineDelta) {
+    // no near tie: rounds 0..k-1 already are the choice (lane k's extra round is dropped below)
+    selected = !(vk - last_v < kRefineDelta);
+    if (!selected) {
 #pragma unroll
       for (int i = 0; i < NPL; ++i) {
         const int e0 = i * 32;
@@ -331,7 +334,8 @@ __device__ void warp_topk_softmax(const float* l, const float* bias, int E, int 
       }
     }
   }
-  warp_select(v, E, k, my_id, my_v, last_v);
+  if (!selected) warp_select(v, E, k, my_id, my_v, last_v);
+  if (lane >= k) { my_id = 0x7fffffff; my_v = -INFINITY; }
   // position of this lane's id among the chosen ids
   int rank = 0;
   for (int j = 0; j < k; ++j) rank += __shfl_sync(0xffffffffu, my_id, j) < my_id ? 1 : 0;
