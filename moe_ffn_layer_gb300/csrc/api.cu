@@ -26,8 +26,13 @@ thread_local int t_last_launches = 0;
 // and the router's tensor-core logits want every SM; forking after the router
 // lets the shared matmuls overlap the top-k, the dispatch and the row copy,
 // which leave the tensor cores idle (measured: prefill T=8192 850 -> 822 us,
-// batched decode T=256 187 -> 180 us; T=16384 +1.6%).
-constexpr int kForkStage = 1;
+// batched decode T=256 187 -> 180 us).  A large router (T*E*H >= 2^33, e.g.
+// T=16384, E=256, H=4096) leaves enough idle SMs of its own that forking
+// before it is better (4507 -> 4403 us there; the T=8192, E=128 prefill loses
+// 759 -> 791 us).
+int fork_stage(const moe_dims* d, int T) {
+  return static_cast<double>(T) * d->E * d->H >= 8589934592.0 ? 0 : 1;
+}
 
 struct DevInfo {
   int* status = nullptr;
@@ -318,15 +323,16 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
                              reinterpret_cast<unsigned int*>(base + L.route_ticket), &dout, di->status, di->sms,
                              stream, &n);
   } else {
-    if (kForkStage == 0) rc = fork_shared();
+    const int fork_at = fork_stage(d, T);
+    if (fork_at == 0) rc = fork_shared();
     if (!rc)
       rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits, nullptr,
                              nullptr, di->status, di->sms, stream, &n);
-    if (!rc && kForkStage == 1) rc = fork_shared();
+    if (!rc && fork_at == 1) rc = fork_shared();
     if (!rc)
       rc = moe::permute_launch(ids, x, T, d->H, d->E, d->k, offsets, sorted, inv, xperm, pcounts, di->status,
                                di->sms, stream, &n);
-    if (!rc && kForkStage == 2) rc = fork_shared();
+    if (!rc && fork_at == 2) rc = fork_shared();
   }
   if (!rc)
     // decode sizes: gmm1 reads the dispatched rows straight from x through

@@ -47,7 +47,7 @@ constexpr int kBK = 64;            // K per stage: one 128-byte swizzle row of b
 constexpr int kThreads = 192;      // 6 warps
 constexpr int kMaxGroups = 1024;
 constexpr int kTileRows128 = 128 * kBK * 2;   // bytes of a 128-row K block
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 216 * 1024;
 
 constexpr int tmem_cols_pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
 
@@ -70,7 +70,11 @@ struct Cfg {
   static constexpr int kAccCols = SWAP ? (ACT == 1 ? 2 : 1) * W : W;             // TMEM columns per unit
   static constexpr int kNumAcc = 2 * kAccCols <= 512 ? 2 : 1;
   static constexpr int kTmemCols = tmem_cols_pow2(kNumAcc * kAccCols);
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256 + 2 * (kMaxGroups + 1) * 4 + 128 * 4;
+  // after the ring: the mbarriers (full/empty per stage, 2 tfull, 2 tempty,
+  // done), the TMEM slot, the abort flag, the unit total and 8 split words
+  static constexpr int kCtrlUsed = (2 * kStages + 5) * 8 + 4 + 4 + 4 + 8 * 4;
+  static constexpr int kCtrlBytes = (kCtrlUsed + 127) / 128 * 128;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes + 2 * (kMaxGroups + 1) * 4 + 128 * 4;
   static_assert(kStages >= 2, "ring too shallow");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
@@ -194,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] mode, [1] last arriver, [2..5] warp ok, [6] P, [7] S
-  int* s_off = reinterpret_cast<int*>(smem + C::kStages * C::kStageBytes + 256);   // [G+1]
+  int* s_off = reinterpret_cast<int*>(smem + C::kStages * C::kStageBytes + C::kCtrlBytes);   // [G+1]
   int* s_ustart = s_off + (kMaxGroups + 1);                                          // [G+1]
   int* s_gidx = s_ustart + (kMaxGroups + 1);                                         // [128] gathered rows
 
