@@ -303,11 +303,12 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
     if (!has_shared) return MOE_OK;
     if (cudaEventRecord(ev_fork, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamWaitEvent(side, ev_fork, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    // (a token adds at most one row to a group: no group holds more than T rows)
     int r = moe::grouped_gemm_launch(x, w->ws_gate_up, nullptr, 1, T, d->I_s, d->H, 1, hs, di->status, &gside,
-                                     side_sms, side, &n);
+                                     side_sms, side, &n, nullptr, 0, 0, T);
     if (!r)
       r = moe::grouped_gemm_launch(hs, w->ws_down, nullptr, 1, T, d->H, d->I_s, 0, s, di->status, &gside,
-                                   side_sms, side, &n);
+                                   side_sms, side, &n, nullptr, 0, 0, T);
     if (r) return r;
     return cudaEventRecord(ev_join, side) != cudaSuccess ? MOE_ERR_CUDA : MOE_OK;
   };
@@ -341,12 +342,12 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
     // cannot feed full 128-row tiles
     rc = T <= moe::route_small_max_tokens()
              ? moe::grouped_gemm_launch(x, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, &gmain,
-                                        main_sms, stream, &n, sorted, T)
+                                        main_sms, stream, &n, sorted, T, 0, T)
              : moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status,
                                         &gmain, di->sms, stream, &n);
   if (!rc)
     rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, &gmain,
-                                  main_sms, stream, &n);
+                                  main_sms, stream, &n, nullptr, 0, 0, T);
   if (rc) return rc;
   // join, then combine
   if (has_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;

@@ -1,0 +1,172 @@
+// Grouped matmul for groups of one token row (decode at T = 1): gmm1
+// (+SiLU*mul) and gmm2 of the MoE FFN layer ("Ascend 910C LLM inference
+// optimisation, part 2" (Dewu Tech), section on MoE multi-stream overlap: the
+// routed path is dispatch -> gmm1 -> gmm2 -> combine), computed on the CUDA
+// cores instead of the tensor cores.
+//
+// With one token row per expert each weight element is used by one
+// multiply-add: the work is a weight stream (HBM-bound), and a tensor-core MMA
+// with 16 token columns would spend its issue slots on padding.  (Measured on
+// GB300: faster than the tensor-core form at one row, slower at two and four,
+// where the per-element unpacking and FMAs start to bind; the kernel keeps a
+// row count R so that the bound stays explicit.)
+// A warp owns one output column of its group (gate and up rows with SiLU*mul)
+// or kRowsDown output columns (plain), reads those weight rows once with
+// 16-byte loads, keeps one fp32 sum per (weight row, token row) per lane, and
+// adds the lanes with a fixed butterfly: deterministic, fp32 accumulation.
+//
+// The grid covers (non-empty group, output block) pairs up to a host bound;
+// every CTA lists the non-empty groups from the device offsets itself.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxGemvGroups = 1024;
+constexpr int kRowsDown = 4;        // output columns per warp without SiLU*mul
+constexpr int kGemvThreads = 256;
+
+__device__ __forceinline__ void bf16x8(const uint4& v, float (&f)[8]) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// ACT 1: out[r][n] = silu(a[r].Wg[n]) * (a[r].Wu[n]), W[g] = [2N][K] (gate rows
+// first); ACT 0: out[r][n] = a[r].W[g][n], W[g] = [N][K].  Token row r of the
+// product is row a_rows[r] of `a` when a_rows is given, else row r.  R >= the
+// rows of any group (1, 2 or 4).
+template <int ACT, int R>
+__global__ void __launch_bounds__(kGemvThreads)
+    grouped_gemv_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ w,
+                        const int32_t* __restrict__ offsets, int G, int rows_max, int N, int K,
+                        const int32_t* __restrict__ a_rows, int a_src_rows, __nv_bfloat16* __restrict__ out,
+                        int* status) {
+  constexpr int NW = ACT == 1 ? 2 : kRowsDown;   // weight rows per warp
+  constexpr int NPW = ACT == 1 ? 1 : kRowsDown;  // output columns per warp
+  __shared__ int s_groups[kMaxGemvGroups];
+  __shared__ int s_count;
+  chain_wait();
+  const ChainReleaseAtExit release_next;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // non-empty groups, in order (a group with more rows than R, or offsets out
+  // of range, is a device-side error: recorded, skipped)
+  if (warp == 0) {
+    int count = 0;
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      bool live = false;
+      if (g < G) {
+        const int lo = offsets ? offsets[g] : 0, hi = offsets ? offsets[g + 1] : rows_max;
+        const bool bad = lo < 0 || hi < lo || hi > rows_max || hi - lo > R;
+        if (bad) set_status(status, MOE_ERR_DEVICE_CHECK);
+        live = !bad && hi > lo;
+      }
+      const uint32_t m = __ballot_sync(0xffffffffu, live);
+      if (live) s_groups[count + __popc(m & ((1u << lane) - 1u))] = g;
+      count += __popc(m);
+    }
+    if (lane == 0) s_count = count;
+  }
+  __syncthreads();
+  const int blocks = N / NPW;                     // output blocks per group
+  const long long item = static_cast<long long>(blockIdx.x) * (kGemvThreads / 32) + warp;
+  if (item >= static_cast<long long>(s_count) * blocks) return;
+  const int g = s_groups[item / blocks];
+  const int n0 = static_cast<int>(item % blocks) * NPW;
+  const int r0 = offsets ? offsets[g] : 0;
+  const int nr = (offsets ? offsets[g + 1] : rows_max) - r0;
+  // this warp's weight rows and token rows (rows past nr repeat the last one)
+  const size_t wrows = ACT == 1 ? 2 * static_cast<size_t>(N) : N;
+  const __nv_bfloat16* wr[NW];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const size_t row = ACT == 1 ? (i == 0 ? n0 : N + n0) : n0 + i;
+    wr[i] = w + (static_cast<size_t>(g) * wrows + row) * K;
+  }
+  const __nv_bfloat16* ar[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    const int r = r0 + (j < nr ? j : nr - 1);
+    int src = a_rows ? a_rows[r] : r;
+    if (src < 0 || src >= (a_rows ? a_src_rows : rows_max)) src = 0;   // checked upstream; never out of range
+    ar[j] = a + static_cast<size_t>(src) * K;
+  }
+  float acc[NW][R];
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+#pragma unroll
+    for (int j = 0; j < R; ++j) acc[i][j] = 0.f;
+#pragma unroll 2
+  for (int k0 = lane * 8; k0 < K; k0 += 256) {
+    uint4 wv[NW], av[R];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) wv[i] = __ldg(reinterpret_cast<const uint4*>(wr[i] + k0));
+#pragma unroll
+    for (int j = 0; j < R; ++j) av[j] = __ldg(reinterpret_cast<const uint4*>(ar[j] + k0));
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      float af[8];
+      bf16x8(av[j], af);
+#pragma unroll
+      for (int i = 0; i < NW; ++i) {
+        float wf[8];
+        bf16x8(wv[i], wf);
+        float s = acc[i][j];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
+        acc[i][j] = s;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
+  if (lane != 0) return;
+#pragma unroll
+  for (int j = 0; j < R; ++j) {
+    if (j >= nr) break;
+    __nv_bfloat16* orow = out + static_cast<size_t>(r0 + j) * N + n0;
+    if (ACT == 1) {
+      const float gt = acc[0][j], up = acc[1][j];
+      orow[0] = __float2bfloat16_rn(gt / (1.0f + __expf(-gt)) * up);
+    } else {
+#pragma unroll
+      for (int i = 0; i < NPW; ++i) orow[i] = __float2bfloat16_rn(acc[i][j]);
+    }
+  }
+}
+
+}  // namespace
+
+bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows) {
+  return max_group_rows == 1 && G <= kMaxGemvGroups && K % 8 == 0 && (act == 1 || N % kRowsDown == 0);
+}
+
+int grouped_gemv_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
+                        int act, void* out, int* status, cudaStream_t stream, int* launches,
+                        const int32_t* a_rows, int a_src_rows, int max_group_rows) {
+  if (rows_max == 0) return MOE_OK;
+  // at most min(G, rows_max) non-empty groups
+  const long long groups = G < rows_max ? G : rows_max;
+  const long long items = groups * (act == 1 ? N : N / kRowsDown);
+  const long long grid = (items + kGemvThreads / 32 - 1) / (kGemvThreads / 32);
+  const __nv_bfloat16* ab = static_cast<const __nv_bfloat16*>(a);
+  const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
+  const dim3 g(static_cast<unsigned>(grid)), b(kGemvThreads);
+  if (max_group_rows != 1) return MOE_ERR_UNSUPPORTED;
+  const cudaError_t rc =
+      act == 1 ? launch_chained(grouped_gemv_kernel<1, 1>, g, b, 0, stream, ab, wb, offsets, G, rows_max, N, K,
+                                a_rows, a_src_rows, ob, status)
+               : launch_chained(grouped_gemv_kernel<0, 1>, g, b, 0, stream, ab, wb, offsets, G, rows_max, N, K,
+                                a_rows, a_src_rows, ob, status);
+  if (rc != cudaSuccess) return MOE_ERR_CUDA;
+  ++*launches;
+  return MOE_OK;
+}
+
+}  // namespace moe

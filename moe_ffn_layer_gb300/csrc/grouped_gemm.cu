@@ -898,9 +898,14 @@ GemmScratch grouped_gemm_scratch(void* ws, size_t ws_bytes) {
 
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, const GemmScratch* scratch, int grid_cap, cudaStream_t stream,
-                        int* launches, const int32_t* a_rows, int a_src_rows, int max_slots) {
+                        int* launches, const int32_t* a_rows, int a_src_rows, int max_slots, int max_group_rows) {
   if (rows_max == 0) return MOE_OK;
   if (max_slots <= 0) max_slots = kMaxSlots;
+  // groups of one row: a weight stream on the CUDA cores
+  const int bound = rows_max == 1 ? 1 : max_group_rows;
+  if (act != 2 && grouped_gemv_applies(G, N, K, act, bound))
+    return grouped_gemv_launch(a, w, offsets, G, rows_max, N, K, act, out, status, stream, launches, a_rows,
+                               a_src_rows, bound);
   if (grouped_gemm_weights_on_m(G, rows_max, N)) {
     if (act == 1)
       return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,

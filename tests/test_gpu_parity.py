@@ -279,6 +279,41 @@ def test_grouped_gemm_shapes_share_one_scratch():
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (G, R, N, K, act)
 
 
+@pytest.mark.parametrize("rows,N,K,act", [
+    ([1, 0, 2, 0, 1], 256, 512, 1), ([1, 0, 2, 0, 1], 512, 256, 0), ([0, 0, 4], 128, 2048, 1),
+    ([1] * 4 + [0] * 60, 768, 2048, 1), ([1] * 4 + [0] * 60, 2048, 768, 0), ([3], 192, 64, 0), ([2, 2], 64, 128, 1),
+    ([0, 1, 0], 768, 2048, 1), ([0, 0, 0, 1], 2048, 768, 0), ([1], 256, 512, 1), ([1], 192, 64, 0)])
+def test_grouped_gemm_groups_of_at_most_four_rows(rows, N, K, act):
+    """Groups of at most four rows with rows_max equal to the rows held (a
+    single row runs on the CUDA cores, more on the tensor cores): every row
+    checked against the oracle, and the call repeats bit for bit."""
+    G = len(rows)
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    R = int(off[-1])
+    a_bits = synth.random_bf16((R, K), seed=R + N + K, tag=57)
+    w_bits = synth.random_bf16((G, 2 * N if act else N, K), seed=K + G, tag=58, sigma=0.05)
+    ref = om.grouped_gemm(a_bits, w_bits, off, act)
+    a = bf16_tensor(a_bits, "cuda")
+    w = bf16_tensor(w_bits, "cuda")
+    out = torch.full((R, N), 1024.0, dtype=torch.bfloat16, device="cuda")
+    B.moe_grouped_gemm(a, w, i32(off), G, R, N, K, act, out, None, 0, stream())
+    no_device_error()
+    got = to_f64(out)
+    assert_close_layer(got, ref, f"small groups rows={rows} N={N} K={K} act={act}")
+    for r in range(R):
+        scale = np.abs(ref[r]).max() + 1e-6
+        assert np.abs(got[r] - ref[r]).max() <= 2e-2 * scale, r
+    out2 = torch.empty_like(out)
+    B.moe_grouped_gemm(a, w, i32(off), G, R, N, K, act, out2, None, 0, stream())
+    no_device_error()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    if G == 1:   # no offsets: one group of R rows
+        out3 = torch.empty_like(out)
+        B.moe_grouped_gemm(a, w, None, 1, R, N, K, act, out3, None, 0, stream())
+        no_device_error()
+        assert torch.equal(out.view(torch.int16), out3.view(torch.int16))
+
+
 def test_grouped_gemm_rejects_bad_offsets():
     """Offsets past rows_max or decreasing: the kernel records a device check
     error and computes nothing."""
