@@ -940,12 +940,21 @@ int router_gemm_launch(const void* x, const void* wr3, int T, int H, int E, floa
                        cudaStream_t stream, int* launches) {
   if (T == 0) return MOE_OK;
   const int K = 3 * H;
-  // narrower N blocks while the row blocks alone would leave SMs idle
+  // the logits block width whose longest CTA streams the fewest bytes: rounds
+  // of units per CTA x (token tile + weight block) per K block
   const long long mtiles = (T + 127) / 128;
-  if (E % 256 == 0 && mtiles * (E / 256) >= grid_cap)
+  int best_bn = 64;
+  long long best = -1;
+  for (int bn = 256; bn >= 64; bn /= 2) {
+    if (E % bn) continue;
+    const long long units = mtiles * (E / bn);
+    const long long cost = (units + grid_cap - 1) / grid_cap * (kTileRows128 + bn * kBK * 2);
+    if (best < 0 || cost < best) { best = cost; best_bn = bn; }
+  }
+  if (best_bn == 256)
     return launch_cfg<0, 256, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, grid_cap, stream, launches,
                                  kMaxSlots, H);
-  if (E % 128 == 0 && mtiles * (E / 128) >= grid_cap)
+  if (best_bn == 128)
     return launch_cfg<0, 128, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, grid_cap, stream, launches,
                                  kMaxSlots, H);
   return launch_cfg<0, 64, 2>(x, wr3, nullptr, 1, T, E, K, logits, status, nullptr, grid_cap, stream, launches,
