@@ -136,9 +136,10 @@ MOE_API int moe_permute(const int32_t* topk_ids, const void* x, int T, int H, in
  *                shapes may use one buffer in turn (sized for the largest).
  *                Calls that share a scratch buffer must not overlap on the GPU.
  * bf16 inputs, fp32 accumulation (in tensor memory; on the CUDA cores when
- * rows_max is 1, a pure weight stream), bf16 (round-to-nearest) output.  With scratch, launches whose groups have at most 16 rows may cut a
- * unit's K range between CTAs (S-way split or stream-K); the partial sums are
- * added in a fixed order, so results do not depend on scheduling.
+ * rows_max is 1, a pure weight stream), bf16 (round-to-nearest) output.  With
+ * scratch, launches whose groups have at most 16 rows may cut a unit's K range
+ * between CTAs (S-way split or stream-K); the partial sums are added in a
+ * fixed order, so results do not depend on scheduling.
  * Supported: K % 64 == 0, N % 64 == 0, G <= 1024. */
 MOE_API size_t moe_grouped_gemm_workspace_bytes(int G, int rows_max, int N, int K, int act);
 MOE_API int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max, int N,
