@@ -20,6 +20,15 @@
 //    but one that adds into the accumulator of the MMA just before it waits
 //    for it, which would cap the weight stream of an SM far below HBM speed.
 //
+// Tokens-on-M launches with an even number of 256-wide weight blocks run as
+// clusters of two CTAs that load one shared operand tile half each and
+// multicast it to both: two 128-row tiles of a group share the weight block,
+// an odd last tile is shared by two adjacent weight blocks.  A ring stage is
+// released once both CTAs' MMAs are done with it.
+//
+// Groups of one row never reach this kernel: they run on the CUDA cores
+// (gemv.cu), a pure weight stream.
+//
 // Roles:  warp 0      TMA producer into a STAGES-deep shared-memory ring
 //         warp 1      tensor-memory allocator and MMA issuer (one thread)
 //         warps 2..5  epilogue: tcgen05.ld -> SiLU*mul or identity -> bf16

@@ -22,9 +22,10 @@
 //             bf16(w - hi - mid); every subtraction is exact in fp32 and the
 //             three terms carry the full 24-bit significand), and since x is
 //             bf16 every product x*term is exact in fp32; the grouped GEMM
-//             adds them in fp32 with K = 3H.  Fewer tokens: fp32 FMAs, one
-//             warp per (expert, 16 tokens) below 512 tokens, else a 64 x 64
-//             SIMT tile GEMM.
+//             adds them in fp32 with K = 3H.  Otherwise fp32 FMAs over up
+//             to 8 slices of H (the top-k adds the slices in slice order):
+//             below 128 tokens one warp per (expert, slice, 16 tokens), from
+//             128 tokens a 64 x 64 SIMT tile GEMM per slice.
 #include "common.cuh"
 #include "kernels.h"
 
