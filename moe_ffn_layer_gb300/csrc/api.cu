@@ -345,13 +345,18 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
                                         main_sms, stream, &n, sorted, T, 0, T)
              : moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status,
                                         &gmain, di->sms, stream, &n);
-  if (!rc)
+  // one token: gmm2 and the combine in one launch, after the join (the shared
+  // expert has long finished by then: it streamed its weights during routing)
+  const bool fused_tail = T == 1 && moe::down_combine_gemv_applies(d->E, d->H, d->I, d->k);
+  if (!rc && !fused_tail)
     rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, &gmain,
                                   main_sms, stream, &n, nullptr, 0, 0, T);
   if (rc) return rc;
   // join, then combine
   if (has_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
-  rc = moe::combine_launch(y, inv, tw, has_shared ? s : nullptr, T, d->H, d->k, rows, out, stream, &n);
+  rc = fused_tail ? moe::down_combine_gemv_launch(h, w->w_down, offsets, d->E, d->H, d->I, d->k, inv, tw,
+                                                  has_shared ? s : nullptr, out, di->status, stream, &n)
+                  : moe::combine_launch(y, inv, tw, has_shared ? s : nullptr, T, d->H, d->k, rows, out, stream, &n);
   t_last_launches = n;
   return rc;
 }

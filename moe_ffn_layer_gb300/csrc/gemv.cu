@@ -24,7 +24,8 @@ namespace moe {
 namespace {
 
 constexpr int kMaxGemvGroups = 1024;
-constexpr int kRowsDown = 4;        // output columns per warp without SiLU*mul
+constexpr int kRowsDown = 2;        // output columns per warp without SiLU*mul
+constexpr int kSteps = 8;           // K strides (256 elements each) whose loads a lane issues together
 constexpr int kGemvThreads = 256;
 
 __device__ __forceinline__ void bf16x8(const uint4& v, float (&f)[8]) {
@@ -97,25 +98,36 @@ __global__ void __launch_bounds__(kGemvThreads)
   for (int i = 0; i < NW; ++i)
 #pragma unroll
     for (int j = 0; j < R; ++j) acc[i][j] = 0.f;
-#pragma unroll 2
-  for (int k0 = lane * 8; k0 < K; k0 += 256) {
-    uint4 wv[NW], av[R];
+  // kSteps strides of K per pass: every load of a pass goes out before its
+  // first FMA (a lane keeps kSteps * (NW + R) 16-byte loads in flight)
+  for (int kb = lane * 8; kb < K; kb += 256 * kSteps) {
+    uint4 wv[kSteps][NW], av[kSteps][R];
 #pragma unroll
-    for (int i = 0; i < NW; ++i) wv[i] = __ldg(reinterpret_cast<const uint4*>(wr[i] + k0));
+    for (int u = 0; u < kSteps; ++u) {
+      const int k0 = kb + u * 256;
+      if (k0 < K) {
 #pragma unroll
-    for (int j = 0; j < R; ++j) av[j] = __ldg(reinterpret_cast<const uint4*>(ar[j] + k0));
+        for (int i = 0; i < NW; ++i) wv[u][i] = __ldg(reinterpret_cast<const uint4*>(wr[i] + k0));
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      float af[8];
-      bf16x8(av[j], af);
+        for (int j = 0; j < R; ++j) av[u][j] = __ldg(reinterpret_cast<const uint4*>(ar[j] + k0));
+      }
+    }
 #pragma unroll
-      for (int i = 0; i < NW; ++i) {
-        float wf[8];
-        bf16x8(wv[i], wf);
-        float s = acc[i][j];
+    for (int u = 0; u < kSteps; ++u) {
+      if (kb + u * 256 >= K) break;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
-        acc[i][j] = s;
+      for (int j = 0; j < R; ++j) {
+        float af[8];
+        bf16x8(av[u][j], af);
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+          float wf[8];
+          bf16x8(wv[u][i], wf);
+          float s = acc[i][j];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
+          acc[i][j] = s;
+        }
       }
     }
   }
@@ -140,7 +152,114 @@ __global__ void __launch_bounds__(kGemvThreads)
   }
 }
 
+// One token (T = 1): gmm2 and the combine in one pass.  Slot j of the token
+// holds row r_j = inv_perm[j], the one row of group g_j; a warp owns output
+// column n and computes every slot's product y_j[n] = h[r_j] . Wd[g_j][n]
+// exactly as the one-row gmm2 above does (lane-strided fp32 sums over K, the
+// same butterfly, rounded to bf16), then out[n] = bf16(sum_j w_j * y_j[n] +
+// shared[n]) with the fp32 adds in slot order, as the combine takes them: the
+// same bits as the two launches, without the round trip of y.
+template <int KC>
+__global__ void __launch_bounds__(kGemvThreads)
+    down_combine_gemv_kernel(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ w,
+                             const int32_t* __restrict__ offsets, int G, int rows, int N, int K, int k,
+                             const int32_t* __restrict__ inv_perm, const float* __restrict__ topk_w,
+                             const __nv_bfloat16* __restrict__ shared, __nv_bfloat16* __restrict__ out,
+                             int* status) {
+  __shared__ int s_group[KC];   // group holding row r, or -1
+  __shared__ int s_row[KC];     // row of slot j, or -1 (adds nothing)
+  __shared__ int s_g[KC];
+  __shared__ float s_w[KC];
+  chain_wait();
+  const ChainReleaseAtExit release_next;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < KC) s_group[threadIdx.x] = -1;
+  __syncthreads();
+  if (warp == 0) {
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      if (g < G) {
+        const int lo = offsets[g], hi = offsets[g + 1];
+        const bool bad = lo < 0 || hi < lo || hi > rows || hi - lo > 1;
+        if (bad) set_status(status, MOE_ERR_DEVICE_CHECK);
+        else if (hi > lo) s_group[lo] = g;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < k) {
+    const int r = inv_perm[threadIdx.x];
+    const int g = (r >= 0 && r < rows) ? s_group[r] : -1;
+    s_row[threadIdx.x] = g >= 0 ? r : -1;
+    s_g[threadIdx.x] = g;
+    s_w[threadIdx.x] = topk_w[threadIdx.x];
+  }
+  __syncthreads();
+  const int n = blockIdx.x * (kGemvThreads / 32) + warp;
+  if (n >= N) return;
+  const __nv_bfloat16* wr[KC];
+  const __nv_bfloat16* hr[KC];
+#pragma unroll
+  for (int j = 0; j < KC; ++j) {
+    const bool live = j < k && s_row[j] >= 0;   // a dead slot re-reads row 0 and is not added
+    wr[j] = w + (static_cast<size_t>(live ? s_g[j] : 0) * N + n) * K;
+    hr[j] = h + static_cast<size_t>(live ? s_row[j] : 0) * K;
+  }
+  float acc[KC];
+#pragma unroll
+  for (int j = 0; j < KC; ++j) acc[j] = 0.f;
+  for (int k0 = lane * 8; k0 < K; k0 += 256) {
+    uint4 wv[KC], hv[KC];
+#pragma unroll
+    for (int j = 0; j < KC; ++j)
+      if (j < k) {
+        wv[j] = __ldg(reinterpret_cast<const uint4*>(wr[j] + k0));
+        hv[j] = __ldg(reinterpret_cast<const uint4*>(hr[j] + k0));
+      }
+#pragma unroll
+    for (int j = 0; j < KC; ++j)
+      if (j < k) {
+        float af[8], wf[8];
+        bf16x8(hv[j], af);
+        bf16x8(wv[j], wf);
+        float s = acc[j];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
+        acc[j] = s;
+      }
+  }
+#pragma unroll
+  for (int j = 0; j < KC; ++j)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+  if (lane != 0) return;
+  float v = 0.f;
+#pragma unroll
+  for (int j = 0; j < KC; ++j)
+    if (j < k && s_row[j] >= 0) v = fmaf(s_w[j], __bfloat162float(__float2bfloat16_rn(acc[j])), v);
+  if (shared) v += __bfloat162float(shared[n]);
+  out[n] = __float2bfloat16_rn(v);
+}
+
 }  // namespace
+
+bool down_combine_gemv_applies(int G, int N, int K, int k) {
+  return k <= 8 && grouped_gemv_applies(G, N, K, 0, 1);
+}
+
+int down_combine_gemv_launch(const void* h, const void* w_down, const int32_t* offsets, int G, int N, int K, int k,
+                             const int32_t* inv_perm, const float* topk_w, const void* shared, void* out,
+                             int* status, cudaStream_t stream, int* launches) {
+  if (k < 1 || k > 8) return MOE_ERR_UNSUPPORTED;
+  const dim3 g((N + kGemvThreads / 32 - 1) / (kGemvThreads / 32)), b(kGemvThreads);
+  const cudaError_t rc = launch_chained(
+      down_combine_gemv_kernel<8>, g, b, 0, stream, static_cast<const __nv_bfloat16*>(h),
+      static_cast<const __nv_bfloat16*>(w_down), offsets, G, k, N, K, k, inv_perm, topk_w,
+      static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(out), status);
+  if (rc != cudaSuccess) return MOE_ERR_CUDA;
+  ++*launches;
+  return MOE_OK;
+}
 
 bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows) {
   return max_group_rows == 1 && G <= kMaxGemvGroups && K % 8 == 0 && (act == 1 || N % kRowsDown == 0);

@@ -64,6 +64,14 @@ bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows);
 int grouped_gemv_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, cudaStream_t stream, int* launches, const int32_t* a_rows,
                         int a_src_rows, int max_group_rows);
+// One token: gmm2 over its k one-row groups and the combine in one launch
+// (out[H] = bf16(sum_j topk_w[j] * y_j + shared)), the same bits as the one-row
+// gmm2 followed by combine_launch.  h: [k][K] rows in group order; shared
+// nullable.  k <= 8.
+bool down_combine_gemv_applies(int G, int N, int K, int k);
+int down_combine_gemv_launch(const void* h, const void* w_down, const int32_t* offsets, int G, int N, int K, int k,
+                             const int32_t* inv_perm, const float* topk_w, const void* shared, void* out,
+                             int* status, cudaStream_t stream, int* launches);
 // logits[T][E] fp32 = x[T][H] . (hi + mid + lo)^T with wr3 = bf16 [E][3H] holding
 // the three bf16 terms of the fp32 router weights in K order (hi | mid | lo);
 // the x tile is re-read for each of the three.  E % 64 == 0, H % 64 == 0.

@@ -503,6 +503,54 @@ def test_forward_matches_standalone_calls(T, H, E, k):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
+@pytest.mark.parametrize("case", ["decode", "no_shared", "k12"])
+def test_forward_one_token_matches_standalone_calls(case):
+    """One token: the layer runs gmm2 and the combine as one launch (k <= 8);
+    its output has the same bits as the standalone calls (route, one-row
+    gate_up and down per slot, the shared expert, combine), and matches the
+    oracle.  k = 12 keeps the two launches."""
+    if case == "decode":
+        wl = synth.workload("decode", 1)
+    elif case == "no_shared":
+        wl = synth.Workload("one", 1, 512, 16, 4, 256, 0, sigma_router=0.1, sigma_w=0.03)
+    else:
+        wl = synth.Workload("one", 1, 256, 32, 12, 128, 64, sigma_router=0.1, sigma_w=0.03)
+    inp = synth.make_inputs(wl, 31)
+    ref = om.forward(inp, wl.k)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    x = bf16_tensor(inp["x"], "cuda")
+    out = L.forward(x).clone()
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], f"one token {case}")
+    H, E, k, I, Is = wl.H, wl.E, wl.k, wl.I, wl.Is
+    wr, bias, wgu, wd, sgu, sd = L.tensors
+    dev = "cuda"
+    ids = torch.empty((1, k), dtype=torch.int32, device=dev)
+    tw = torch.empty((1, k), dtype=torch.float32, device=dev)
+    rb = B.moe_route_workspace_bytes(1, H, E)
+    rws = torch.empty(max(rb, 256), dtype=torch.uint8, device=dev)
+    B.moe_route(x, wr, bias, 1, H, E, k, ids, tw, rws, rb, stream())
+    nb = max(B.moe_grouped_gemm_workspace_bytes(1, 1, n_, k_, a_)
+             for n_, k_, a_ in [(I, H, 1), (H, I, 0), (max(Is, 64), H, 1), (H, max(Is, 64), 0)])
+    gws = torch.zeros(max(nb, 256), dtype=torch.uint8, device=dev)
+    y = torch.empty((k, H), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((1, I), dtype=torch.bfloat16, device=dev)
+    for j, g in enumerate(ids[0].tolist()):
+        B.moe_grouped_gemm(x, wgu[g:g + 1], None, 1, 1, I, H, 1, h, gws, nb, stream())
+        B.moe_grouped_gemm(h, wd[g:g + 1], None, 1, 1, H, I, 0, y[j:j + 1], gws, nb, stream())
+    sh = None
+    if Is:
+        hs = torch.empty((1, Is), dtype=torch.bfloat16, device=dev)
+        sh = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+        B.moe_grouped_gemm(x, sgu, None, 1, 1, Is, H, 1, hs, gws, nb, stream())
+        B.moe_grouped_gemm(hs, sd, None, 1, 1, H, Is, 0, sh, gws, nb, stream())
+    out2 = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+    inv = torch.arange(k, dtype=torch.int32, device=dev)   # y is in slot order
+    B.moe_unpermute_combine(y, inv, tw, sh, 1, H, k, out2, stream())
+    no_device_error()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
 def test_forward_repeatable_and_launch_count():
     """Two calls give identical bits; the launch count is what the call reports."""
     L = layer("tiny", 16)
