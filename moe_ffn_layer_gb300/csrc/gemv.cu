@@ -33,6 +33,61 @@ __device__ __forceinline__ void bf16x8(const uint4& v, float (&f)[8]) {
   f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
+// The non-empty groups in ascending order into s_groups, their number into
+// *s_count (every thread of the CTA takes part; one round of offset loads).  A
+// group with more rows than max_rows, or offsets out of range, is a device-side
+// error: recorded, skipped.  Without offsets the one group holds rows_max rows.
+__device__ __forceinline__ void list_groups(const int32_t* __restrict__ offsets, int G, int rows_max, int max_rows,
+                                            int* status, int* s_groups, int* s_count) {
+  constexpr int kChunks = kMaxGemvGroups / kGemvThreads;
+  constexpr int kWarps = kGemvThreads / 32;
+  static_assert(kChunks * kWarps == 32, "one warp scans the (chunk, warp) counts");
+  __shared__ int s_base[kChunks * kWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int lo[kChunks], hi[kChunks];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int g = c * kGemvThreads + threadIdx.x;
+    lo[c] = 0;
+    hi[c] = 0;
+    if (g < G) {
+      lo[c] = offsets ? __ldg(offsets + g) : 0;
+      hi[c] = offsets ? __ldg(offsets + g + 1) : rows_max;
+    }
+  }
+  uint32_t mask[kChunks];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int g = c * kGemvThreads + threadIdx.x;
+    bool live = false;
+    if (g < G) {
+      const bool bad = lo[c] < 0 || hi[c] < lo[c] || hi[c] > rows_max || hi[c] - lo[c] > max_rows;
+      if (bad) set_status(status, MOE_ERR_DEVICE_CHECK);
+      live = !bad && hi[c] > lo[c];
+    }
+    mask[c] = __ballot_sync(0xffffffffu, live);
+    if (lane == 0) s_base[c * kWarps + warp] = __popc(mask[c]);
+  }
+  __syncthreads();
+  if (warp == 0) {   // exclusive prefix over (chunk, warp) = ascending group order
+    const int v = s_base[lane];
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    s_base[lane] = incl - v;
+    if (lane == 31) *s_count = incl;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c)
+    if (mask[c] >> lane & 1u)
+      s_groups[s_base[c * kWarps + warp] + __popc(mask[c] & ((1u << lane) - 1u))] = c * kGemvThreads + threadIdx.x;
+  __syncthreads();
+}
+
 // ACT 1: out[r][n] = silu(a[r].Wg[n]) * (a[r].Wu[n]), W[g] = [2N][K] (gate rows
 // first); ACT 0: out[r][n] = a[r].W[g][n], W[g] = [N][K].  Token row r of the
 // product is row a_rows[r] of `a` when a_rows is given, else row r.  R >= the
@@ -50,29 +105,11 @@ __global__ void __launch_bounds__(kGemvThreads)
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // non-empty groups, in order (a group with more rows than R, or offsets out
-  // of range, is a device-side error: recorded, skipped)
-  if (warp == 0) {
-    int count = 0;
-    for (int g0 = 0; g0 < G; g0 += 32) {
-      const int g = g0 + lane;
-      bool live = false;
-      if (g < G) {
-        const int lo = offsets ? offsets[g] : 0, hi = offsets ? offsets[g + 1] : rows_max;
-        const bool bad = lo < 0 || hi < lo || hi > rows_max || hi - lo > R;
-        if (bad) set_status(status, MOE_ERR_DEVICE_CHECK);
-        live = !bad && hi > lo;
-      }
-      const uint32_t m = __ballot_sync(0xffffffffu, live);
-      if (live) s_groups[count + __popc(m & ((1u << lane) - 1u))] = g;
-      count += __popc(m);
-    }
-    if (lane == 0) s_count = count;
-  }
-  __syncthreads();
+  list_groups(offsets, G, rows_max, R, status, s_groups, &s_count);
   const int blocks = N / NPW;                     // output blocks per group
-  const long long item = static_cast<long long>(blockIdx.x) * (kGemvThreads / 32) + warp;
-  if (item >= static_cast<long long>(s_count) * blocks) return;
+  const long long items = static_cast<long long>(s_count) * blocks;
+  for (long long item = static_cast<long long>(blockIdx.x) * (kGemvThreads / 32) + warp; item < items;
+       item += static_cast<long long>(gridDim.x) * (kGemvThreads / 32)) {
   const int g = s_groups[item / blocks];
   const int n0 = static_cast<int>(item % blocks) * NPW;
   const int r0 = offsets ? offsets[g] : 0;
@@ -137,123 +174,131 @@ __global__ void __launch_bounds__(kGemvThreads)
     for (int j = 0; j < R; ++j)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
-  if (lane != 0) return;
+  if (lane == 0) {
 #pragma unroll
-  for (int j = 0; j < R; ++j) {
-    if (j >= nr) break;
-    __nv_bfloat16* orow = out + static_cast<size_t>(r0 + j) * N + n0;
-    if (ACT == 1) {
-      const float gt = acc[0][j], up = acc[1][j];
-      orow[0] = __float2bfloat16_rn(gt / (1.0f + __expf(-gt)) * up);
-    } else {
+    for (int j = 0; j < R; ++j) {
+      if (j >= nr) break;
+      __nv_bfloat16* orow = out + static_cast<size_t>(r0 + j) * N + n0;
+      if (ACT == 1) {
+        const float gt = acc[0][j], up = acc[1][j];
+        orow[0] = __float2bfloat16_rn(gt / (1.0f + __expf(-gt)) * up);
+      } else {
 #pragma unroll
-      for (int i = 0; i < NPW; ++i) orow[i] = __float2bfloat16_rn(acc[i][j]);
+        for (int i = 0; i < NPW; ++i) orow[i] = __float2bfloat16_rn(acc[i][j]);
+      }
     }
+  }
   }
 }
 
 // One token (T = 1): gmm2 and the combine in one pass.  Slot j of the token
-// holds row r_j = inv_perm[j], the one row of group g_j; a warp owns output
-// column n and computes every slot's product y_j[n] = h[r_j] . Wd[g_j][n]
-// exactly as the one-row gmm2 above does (lane-strided fp32 sums over K, the
-// same butterfly, rounded to bf16), then out[n] = bf16(sum_j w_j * y_j[n] +
+// holds row r_j = inv_perm[j], the one row of group g_j.  A CTA owns kTailCols
+// consecutive output columns and warp j slot j: the warp reads its h row once
+// and the kTailCols weight rows Wd[g_j][n] (contiguous), with kTailSteps K
+// strides of loads in flight, and computes y_j[n] = h[r_j] . Wd[g_j][n] exactly
+// as the one-row gmm2 above does (lane-strided fp32 sums over K, the same
+// butterfly, rounded to bf16).  Then out[n] = bf16(sum_j w_j * y_j[n] +
 // shared[n]) with the fp32 adds in slot order, as the combine takes them: the
 // same bits as the two launches, without the round trip of y.
-template <int KC>
+constexpr int kTailCols = 4;
+constexpr int kTailSteps = 4;
+constexpr int kTailSlots = kGemvThreads / 32;   // one warp per slot
+
 __global__ void __launch_bounds__(kGemvThreads)
     down_combine_gemv_kernel(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ w,
                              const int32_t* __restrict__ offsets, int G, int rows, int N, int K, int k,
                              const int32_t* __restrict__ inv_perm, const float* __restrict__ topk_w,
                              const __nv_bfloat16* __restrict__ shared, __nv_bfloat16* __restrict__ out,
                              int* status) {
-  __shared__ int s_group[KC];   // group holding row r, or -1
-  __shared__ int s_row[KC];     // row of slot j, or -1 (adds nothing)
-  __shared__ int s_g[KC];
-  __shared__ float s_w[KC];
+  __shared__ int s_group[kTailSlots];            // group holding row r (rows <= k), or -1
+  __shared__ float s_y[kTailSlots][kTailCols];   // y_j[n], bf16-rounded
+  __shared__ int s_live[kTailSlots];
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x < KC) s_group[threadIdx.x] = -1;
+  if (threadIdx.x < kTailSlots) s_group[threadIdx.x] = -1;
   __syncthreads();
-  if (warp == 0) {
-    for (int g0 = 0; g0 < G; g0 += 32) {
-      const int g = g0 + lane;
-      if (g < G) {
-        const int lo = offsets[g], hi = offsets[g + 1];
-        const bool bad = lo < 0 || hi < lo || hi > rows || hi - lo > 1;
-        if (bad) set_status(status, MOE_ERR_DEVICE_CHECK);
-        else if (hi > lo) s_group[lo] = g;
+  for (int g = threadIdx.x; g < G; g += kGemvThreads) {
+    const int lo = __ldg(offsets + g), hi = __ldg(offsets + g + 1);
+    const bool bad = lo < 0 || hi < lo || hi > rows || hi - lo > 1;
+    if (bad) set_status(status, MOE_ERR_DEVICE_CHECK);
+    else if (hi > lo) s_group[lo] = g;
+  }
+  __syncthreads();
+  const int n0 = blockIdx.x * kTailCols;
+  const int j = warp;
+  if (j < k) {
+    const int r = __ldg(inv_perm + j);
+    const int g = (r >= 0 && r < rows) ? s_group[r] : -1;   // a row no group holds adds nothing
+    float acc[kTailCols];
+#pragma unroll
+    for (int c = 0; c < kTailCols; ++c) acc[c] = 0.f;
+    if (g >= 0) {
+      const __nv_bfloat16* hr = h + static_cast<size_t>(r) * K;
+      const __nv_bfloat16* wr = w + (static_cast<size_t>(g) * N + n0) * K;
+      for (int kb = lane * 8; kb < K; kb += 256 * kTailSteps) {
+        uint4 wv[kTailSteps][kTailCols], hv[kTailSteps];
+#pragma unroll
+        for (int u = 0; u < kTailSteps; ++u) {
+          const int k0 = kb + u * 256;
+          if (k0 < K) {
+            hv[u] = __ldg(reinterpret_cast<const uint4*>(hr + k0));
+#pragma unroll
+            for (int c = 0; c < kTailCols; ++c)
+              wv[u][c] = __ldg(reinterpret_cast<const uint4*>(wr + static_cast<size_t>(c) * K + k0));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kTailSteps; ++u) {
+          if (kb + u * 256 >= K) break;
+          float af[8];
+          bf16x8(hv[u], af);
+#pragma unroll
+          for (int c = 0; c < kTailCols; ++c) {
+            float wf[8];
+            bf16x8(wv[u][c], wf);
+            float s = acc[c];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
+            acc[c] = s;
+          }
+        }
       }
+#pragma unroll
+      for (int c = 0; c < kTailCols; ++c)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], o);
+    }
+    if (lane == 0) {
+      s_live[j] = g >= 0;
+#pragma unroll
+      for (int c = 0; c < kTailCols; ++c) s_y[j][c] = __bfloat162float(__float2bfloat16_rn(acc[c]));
     }
   }
   __syncthreads();
-  if (threadIdx.x < k) {
-    const int r = inv_perm[threadIdx.x];
-    const int g = (r >= 0 && r < rows) ? s_group[r] : -1;
-    s_row[threadIdx.x] = g >= 0 ? r : -1;
-    s_g[threadIdx.x] = g;
-    s_w[threadIdx.x] = topk_w[threadIdx.x];
+  if (threadIdx.x < kTailCols && n0 + static_cast<int>(threadIdx.x) < N) {
+    const int n = n0 + threadIdx.x;
+    float v = 0.f;
+    for (int s = 0; s < k; ++s)
+      if (s_live[s]) v = fmaf(__ldg(topk_w + s), s_y[s][threadIdx.x], v);
+    if (shared) v += __bfloat162float(shared[n]);
+    out[n] = __float2bfloat16_rn(v);
   }
-  __syncthreads();
-  const int n = blockIdx.x * (kGemvThreads / 32) + warp;
-  if (n >= N) return;
-  const __nv_bfloat16* wr[KC];
-  const __nv_bfloat16* hr[KC];
-#pragma unroll
-  for (int j = 0; j < KC; ++j) {
-    const bool live = j < k && s_row[j] >= 0;   // a dead slot re-reads row 0 and is not added
-    wr[j] = w + (static_cast<size_t>(live ? s_g[j] : 0) * N + n) * K;
-    hr[j] = h + static_cast<size_t>(live ? s_row[j] : 0) * K;
-  }
-  float acc[KC];
-#pragma unroll
-  for (int j = 0; j < KC; ++j) acc[j] = 0.f;
-  for (int k0 = lane * 8; k0 < K; k0 += 256) {
-    uint4 wv[KC], hv[KC];
-#pragma unroll
-    for (int j = 0; j < KC; ++j)
-      if (j < k) {
-        wv[j] = __ldg(reinterpret_cast<const uint4*>(wr[j] + k0));
-        hv[j] = __ldg(reinterpret_cast<const uint4*>(hr[j] + k0));
-      }
-#pragma unroll
-    for (int j = 0; j < KC; ++j)
-      if (j < k) {
-        float af[8], wf[8];
-        bf16x8(hv[j], af);
-        bf16x8(wv[j], wf);
-        float s = acc[j];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
-        acc[j] = s;
-      }
-  }
-#pragma unroll
-  for (int j = 0; j < KC; ++j)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
-  if (lane != 0) return;
-  float v = 0.f;
-#pragma unroll
-  for (int j = 0; j < KC; ++j)
-    if (j < k && s_row[j] >= 0) v = fmaf(s_w[j], __bfloat162float(__float2bfloat16_rn(acc[j])), v);
-  if (shared) v += __bfloat162float(shared[n]);
-  out[n] = __float2bfloat16_rn(v);
 }
 
 }  // namespace
 
 bool down_combine_gemv_applies(int G, int N, int K, int k) {
-  return k <= 8 && grouped_gemv_applies(G, N, K, 0, 1);
+  return k <= kTailSlots && N % kTailCols == 0 && grouped_gemv_applies(G, N, K, 0, 1);
 }
 
 int down_combine_gemv_launch(const void* h, const void* w_down, const int32_t* offsets, int G, int N, int K, int k,
                              const int32_t* inv_perm, const float* topk_w, const void* shared, void* out,
                              int* status, cudaStream_t stream, int* launches) {
-  if (k < 1 || k > 8) return MOE_ERR_UNSUPPORTED;
-  const dim3 g((N + kGemvThreads / 32 - 1) / (kGemvThreads / 32)), b(kGemvThreads);
+  if (k < 1 || k > kTailSlots || N % kTailCols) return MOE_ERR_UNSUPPORTED;
+  const dim3 g(N / kTailCols), b(kGemvThreads);
   const cudaError_t rc = launch_chained(
-      down_combine_gemv_kernel<8>, g, b, 0, stream, static_cast<const __nv_bfloat16*>(h),
+      down_combine_gemv_kernel, g, b, 0, stream, static_cast<const __nv_bfloat16*>(h),
       static_cast<const __nv_bfloat16*>(w_down), offsets, G, k, N, K, k, inv_perm, topk_w,
       static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(out), status);
   if (rc != cudaSuccess) return MOE_ERR_CUDA;
@@ -272,17 +317,23 @@ int grouped_gemv_launch(const void* a, const void* w, const int32_t* offsets, in
   // at most min(G, rows_max) non-empty groups
   const long long groups = G < rows_max ? G : rows_max;
   const long long items = groups * (act == 1 ? N : N / kRowsDown);
-  const long long grid = (items + kGemvThreads / 32 - 1) / (kGemvThreads / 32);
-  const __nv_bfloat16* ab = static_cast<const __nv_bfloat16*>(a);
-  const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
-  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
-  const dim3 g(static_cast<unsigned>(grid)), b(kGemvThreads);
   if (max_group_rows != 1) return MOE_ERR_UNSUPPORTED;
-  const cudaError_t rc =
-      act == 1 ? launch_chained(grouped_gemv_kernel<1, 1>, g, b, 0, stream, ab, wb, offsets, G, rows_max, N, K,
-                                a_rows, a_src_rows, ob, status)
-               : launch_chained(grouped_gemv_kernel<0, 1>, g, b, 0, stream, ab, wb, offsets, G, rows_max, N, K,
-                                a_rows, a_src_rows, ob, status);
+  auto kernel = act == 1 ? grouped_gemv_kernel<1, 1> : grouped_gemv_kernel<0, 1>;
+  // persistent: no more CTAs than stay resident (each lists the groups once)
+  long long grid = (items + kGemvThreads / 32 - 1) / (kGemvThreads / 32);
+  int* dev_status = nullptr;
+  int sms = 0;
+  static int occupancy[2] = {0, 0};   // resident CTAs per SM of each form (looked up once)
+  int& per_sm = occupancy[act == 1];
+  if (current_device_info(&dev_status, &sms) != MOE_OK) return MOE_ERR_CUDA;
+  if (per_sm == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kGemvThreads, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const long long resident = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
+  if (grid > resident) grid = resident;
+  const dim3 g(static_cast<unsigned>(grid)), b(kGemvThreads);
+  const cudaError_t rc = launch_chained(kernel, g, b, 0, stream, static_cast<const __nv_bfloat16*>(a),
+                                        static_cast<const __nv_bfloat16*>(w), offsets, G, rows_max, N, K, a_rows,
+                                        a_src_rows, static_cast<__nv_bfloat16*>(out), status);
   if (rc != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
