@@ -12,11 +12,14 @@
 // row count R so that the bound stays explicit.)
 // A warp owns one output column of its group (gate and up rows with SiLU*mul)
 // or kRowsDown output columns (plain), reads those weight rows once with
-// 16-byte loads, keeps one fp32 sum per (weight row, token row) per lane, and
-// adds the lanes with a fixed butterfly: deterministic, fp32 accumulation.
+// 16-byte loads (kSteps strides of K in flight), keeps one fp32 sum per
+// (weight row, token row) per lane, and adds the lanes with a fixed butterfly:
+// deterministic, fp32 accumulation.
 //
-// The grid covers (non-empty group, output block) pairs up to a host bound;
-// every CTA lists the non-empty groups from the device offsets itself.
+// At one token the step is latency-bound, so the grid is persistent (resident
+// CTAs walk the (non-empty group, output block) items) and each CTA lists the
+// non-empty groups once, with all offsets loaded in one round.  For one token
+// gmm2 and the combine also run as one launch (down_combine_gemv_kernel).
 #include "common.cuh"
 #include "kernels.h"
 
