@@ -205,7 +205,6 @@ __global__ void __launch_bounds__(256)
 // b[e]) and the selection is run again.  The tensor-core logits differ from
 // fp32 ones by far less than kRefineDelta / 2, so experts outside that band
 // keep their side of the boundary and the choice equals the fp32 choice.
-constexpr int kTopkMaxPerLane = kMaxExperts / 32;
 constexpr float kRefineDelta = 5e-4f;
 
 struct Refine {
