@@ -179,7 +179,9 @@ MOE_API int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const 
 /* The whole layer: route -> permute -> gmm1(+SiLU*mul) -> gmm2 on `stream`;
  * the shared expert's two matmuls on `side` between ev_fork (recorded on
  * `stream`, waited by `side`) and ev_join (recorded on `side`, waited by
- * `stream` before the combine).  Exactly one fork and one join event per call.
+ * `stream` before the combine; for one token with k <= 8, gmm2 and the
+ * combine are one launch and the join comes before it).  Exactly one fork and
+ * one join event per call.
  * `side` and the events may be NULL when d->I_s == 0.  ws holds every
  * intermediate and the split-K scratch of the four matmuls; size it with
  * moe_workspace_bytes(d, T), align it to 256 bytes and zero-fill it before its
