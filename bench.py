@@ -1,31 +1,43 @@
-"""Benchmark of the MoE FFN layer forward on GB300: MoE-layer tokens/s and the
-roofline fraction of the dominant kernel.
+"""Benchmark of the MoE FFN layer forward on one GB300: MoE-layer tokens/s and
+the roofline fraction of the layer and of its dominant kernel.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode --T 8] [--impl reference]
+    python bench.py [--steps K] [--warmup W] [--workload decode --T 8] [--no-sweep] [--impl reference]
 
 A step is one whole-layer forward (route, dispatch, gate_up GroupedMatmul with
 SiLU*mul, down GroupedMatmul, combine, shared expert on the side stream) over
 one batch of T synthetic tokens.  Inputs are seeded and synthetic with the
 workload's shapes and distributions.  Expert weights rotate over R device
-copies so that every step streams its experts' weights from HBM rather than L2.
-One forward per copy is captured in a CUDA graph and the graphs are replayed
+copies so that every step streams its experts' weights from HBM rather than
+L2.  One forward per copy is captured in a CUDA graph (its output first
+checked bit for bit against the eager forward) and the graphs are replayed
 back to back; K replays are timed with CUDA events on the launching stream.
 
-Under torchrun (N > 1) each rank runs its own replica of the layer on its GPU
-(the layer does not shard: replicas only); rank 0 prints one JSON line with
-value = tokens of all ranks / max time over ranks.
+The headline line is the named workload (default: decode T=8) timed over
+exactly K steps.  Unless --no-sweep is given, the line also carries
+``workloads``: every decode, batched-decode and prefill shape of the metric,
+each timed over its own step count (about a quarter second of replays), with
+its layer roofline, its dominant kernel's roofline and the clock samples of
+its own timed window.  Clocks are sampled every 20 ms over the whole
+measurement phase.
 
-``--impl reference`` times the CPU oracle instead (rank 0 only), on bounded
-samples of the same workload.
+One GPU only: the layer does not shard, and its prefill matmuls share operand
+tiles between the two CTAs of a cluster by TMA multicast, which stays inside
+one GPU's own memory.  ``--gpus N`` with N > 1 (or WORLD_SIZE > 1) is refused
+before anything is built or loaded.
+
+``--impl reference`` times the CPU oracle instead, on bounded samples of the
+same workload (rank 0 only under torchrun).
 """
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -36,9 +48,14 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s (decode T=1..256, prefill T=8K) and % of HBM/TC roofline"
 UNIT = "tokens/s"
-DEFAULT_STEPS = {"tiny": 2000, "decode": 4000, "batched_decode": 2000, "prefill": 300, "large_prefill": 60}
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# every shape of the metric, timed after the headline unless --no-sweep
+SWEEP = [("decode", 1), ("decode", 4), ("decode", 8), ("batched_decode", 64), ("batched_decode", 256),
+         ("prefill", 8192), ("large_prefill", 16384)]
+SWEEP_SECONDS = 0.25          # timed replays per sweep workload
+ONE_GPU = ("one GPU only: the layer does not shard, and its prefill matmuls share operand tiles between the two "
+           "CTAs of a cluster by TMA multicast, which stays inside one GPU's own memory")
 
 
 def peaks():
@@ -60,6 +77,14 @@ def layer_units(w, nonempty):
     return bytes_, flops
 
 
+def routed_units(w, nonempty):
+    """The routed path alone (router, dispatch, both routed matmuls, combine):
+    weights of the non-empty experts, the router weights, x and out."""
+    bytes_ = 6 * w.H * w.I * nonempty + 4 * w.E * w.H + 2 * w.T * w.H * 2
+    flops = 2 * w.T * w.k * 3 * w.H * w.I + 2 * w.T * w.E * w.H
+    return bytes_, flops
+
+
 def gate_up_units(w, nonempty):
     """gate_up GroupedMatmul: reads the 2I x H weights of each non-empty expert
     and the T*k dispatched rows, writes T*k rows of h."""
@@ -69,90 +94,90 @@ def gate_up_units(w, nonempty):
     return bytes_, flops
 
 
+def tokens_per_s(tokens_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput of `steps` steps of `tokens_per_step` tokens in `ms`."""
+    return steps * tokens_per_step / (ms / 1e3)
+
+
+def weight_copies(w) -> tuple[int, int]:
+    """(R, touched bytes): R device copies of the expert weights, enough that R
+    x the bytes one forward touches is at least 4 x L2."""
+    wgt_bytes = 3 * w.I * w.H * 2
+    touched = min(w.E, w.T * w.k) * wgt_bytes + 6 * w.H * w.Is
+    return int(min(16, max(2, -(-4 * L2_BYTES // max(touched, 1))))), touched
+
+
+def _routing_desc(w):
+    if w.zipf_s is None and not w.n_empty:
+        return f"router W ~ N(0,{w.sigma_router}), near-uniform"
+    s = f"router W ~ N(0,{w.sigma_router}) + Zipf(s={w.zipf_s}) log-rank bias"
+    return s + (f", {w.n_empty} experts forced empty" if w.n_empty else "")
+
+
+def config_of(w) -> dict:
+    """The workload's config dict (the same for both arms)."""
+    R, touched = weight_copies(w)
+    return {"workload": f"{w.name.split('@')[0]} T={w.T}", "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
+            "I_s": w.Is, "routing": _routing_desc(w), "parallelism": "one GPU (the layer does not shard)",
+            "l2": f"expert weights rotate over {R} device copies ({R} x {touched / 1e6:.0f} MB touched >= 4 x L2); "
+                  f"one CUDA graph per copy, replayed back to back"}
+
+
 # ---------------------------------------------------------------- clocks
 
-CLOCK_Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-           "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-           "clocks_event_reasons.sw_power_cap")
+CLOCK_Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+           "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+           "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+_REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
 
 class ClockSampler:
-    def __init__(self, index: int):
+    """nvidia-smi samples every 20 ms for the whole measurement phase; window()
+    summarises the samples whose own timestamps fall in a host-time window."""
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.samples = []
         self.proc = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_Q}", "--format=csv,noheader,nounits",
-                                          "-i", str(index), "-lms", "100"], stdout=subprocess.PIPE,
-                                         stderr=subprocess.DEVNULL, text=True)
+                                          "-i", str(index), "-lms", str(period_ms)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except OSError:
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, mx, pw, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+    def _read(self):
+        for line in self.proc.stdout:
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-                pw.append(float(f[2]))
+                t = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx, pw = float(f[1]), float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
+            active = [n for n, v in zip(_REASONS, f[5:9]) if v.lower() == "active"]
+            self.samples.append((t, sm, mx, pw, active))
 
+    def window(self, t0: float, t1: float, pad: float = 0.0) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        s = [x for x in list(self.samples) if t0 - pad <= x[0] <= t1 + pad]
+        reasons = sorted({r for x in s for r in x[4]})
+        return {"sm_mhz": statistics.median(x[1] for x in s) if s else None,
+                "sm_max_mhz": max(x[2] for x in s) if s else None,
+                "power_w_max": max(x[3] for x in s) if s else None, "reasons": reasons, "samples": len(s),
+                "window_s": round(t1 - t0 + 2 * pad, 3)}
 
-# ---------------------------------------------------------------- distributed
-
-def dist_setup(n_gpus):
-    import torch
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    return rank, world, local
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(v: float, world: int) -> float:
-    """Largest value over all ranks (the slowest rank's time)."""
-    if world == 1:
-        return v
-    import torch
-    import torch.distributed as dist
-    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
-    t = torch.tensor([v], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def whole_job(ms_local: float, tokens_per_rank: int, steps: int, world: int):
-    """(tokens/s of all ranks together, ms of the slowest rank) for `steps`
-    timed steps of `tokens_per_rank` tokens on every rank."""
-    ms = max_over_ranks(ms_local, world)
-    return world * steps * tokens_per_rank / (ms / 1e3), ms
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -179,42 +204,87 @@ def time_oracle(w, inp, budget_s: float, max_tokens: int | None = None):
     return done / el, cores, done, el
 
 
-# ---------------------------------------------------------------- main arm
+# ---------------------------------------------------------------- GPU arm
 
-def run_gpu(args, w):
+class WeightBed:
+    """Device copies of one set of expert and shared weights; workloads with
+    the same layer sizes (decode, batched decode and prefill) share them."""
+
+    def __init__(self, w, seed, dev):
+        import torch
+
+        from moe_ffn_layer_gb300 import synth
+        from moe_ffn_layer_gb300.layer import bf16_tensor
+        self.dev = dev
+        wgu, wd = synth.make_expert_weights(w, seed)
+        sgu, sd = synth.make_shared_weights(w, seed)
+        self.host = dict(w_gate_up=wgu, w_down=wd, ws_gate_up=sgu, ws_down=sd)
+        b16 = lambda a: None if a is None else bf16_tensor(a, dev)
+        self.copies = [(b16(wgu), b16(wd), b16(sgu), b16(sd))]
+        self._torch = torch
+
+    def get(self, R):
+        while len(self.copies) < R:
+            t = self.copies[0]
+            self.copies.append(tuple(None if a is None else a.clone() for a in t))
+        return self.copies[:R]
+
+
+def _timed_graph(graphs, stream, K, e0, e1, pre_s=0.0, post_s=0.0):
+    """Replays graphs[i % R] K times between two events; optional untimed
+    replays before and after (host-time bounded) keep the load steady around
+    the timed region.  Returns (ms, t_start, t_end) in host time."""
+    R = len(graphs)
+    t_pre = time.time()
+    if pre_s > 0:
+        i = 0
+        while time.time() - t_pre < pre_s:
+            for _ in range(64):
+                graphs[i % R].replay()
+                i += 1
+            stream.synchronize()
+    e0.record(stream)
+    for i in range(K):
+        graphs[i % R].replay()
+    e1.record(stream)
+    e1.synchronize()
+    t_post = time.time()
+    if post_s > 0:
+        i = 0
+        while time.time() - t_post < post_s:
+            for _ in range(64):
+                graphs[i % R].replay()
+                i += 1
+            stream.synchronize()
+    return e0.elapsed_time(e1), t_pre, time.time()
+
+
+def measure(w, bed, args, clk, K, W, headline=False):
     import torch
 
     from moe_ffn_layer_gb300 import binding as B
-    from moe_ffn_layer_gb300 import build as build_mod
     from moe_ffn_layer_gb300 import synth
     from moe_ffn_layer_gb300.layer import MoEFFN, bf16_tensor
 
-    build_mod.build()
-    rank, world, local = dist_setup(args.gpus)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    inp = synth.make_inputs(w, args.seed)
-    base = MoEFFN.from_inputs(inp, w.k, dev)
-    x = bf16_tensor(inp["x"], dev)
-
-    # weight copies: R x touched bytes >= 4 x L2
-    wgt_bytes = (2 * w.I * w.H + w.H * w.I) * 2
-    touched = min(w.E, w.T * w.k) * wgt_bytes + 6 * w.H * w.Is
-    R = int(min(16, max(2, -(-4 * L2_BYTES // max(touched, 1)))))
+    dev = bed.dev
+    x_np, wr_np, b_np = synth.make_activations(w, args.seed)
+    x = bf16_tensor(x_np, dev)
+    wr = torch.from_numpy(wr_np).to(dev)
+    b = None if b_np is None else torch.from_numpy(b_np).to(dev)
+    R, _ = weight_copies(w)
     if args.copies:
         R = args.copies
-    layers = [base]
-    for _ in range(R - 1):
-        t = base.tensors
-        layers.append(MoEFFN(w.k, t[0], t[1], t[2].clone(), t[3].clone(),
-                             None if t[4] is None else t[4].clone(), None if t[5] is None else t[5].clone()))
+    copies = bed.get(R)
+    layers = [MoEFFN(w.k, wr, b, *c) for c in copies]
     outs = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
-        for L, o in zip(layers, outs):          # eager warm-up (sets kernel attributes, sizes workspaces)
+        for L, o in zip(layers, outs):          # eager forwards (set kernel attributes, size workspaces)
             L.forward(x, o, stream)
     stream.synchronize()
     launches = B.moe_last_launch_count()
     assert B.moe_last_device_error(stream) == 0
+    eager0 = outs[0].clone()
     graphs = []
     for L, o in zip(layers, outs):
         g = torch.cuda.CUDAGraph()
@@ -222,159 +292,207 @@ def run_gpu(args, w):
             L.forward(x, o, torch.cuda.current_stream())
         graphs.append(g)
     torch.cuda.synchronize()
+    outs[0].fill_(0)
+    with torch.cuda.stream(stream):
+        graphs[0].replay()
+    stream.synchronize()
+    graph_same = bool(torch.equal(outs[0].view(torch.int16), eager0.view(torch.int16)))
 
-    K, W = args.steps, args.warmup
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for i in range(W):
             graphs[i % R].replay()
-    stream.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    clk = ClockSampler(local) if rank == 0 else None
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(K):
-            graphs[i % R].replay()
-        e1.record(stream)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    clocks = clk.stop() if clk else None
-    barrier(world)
-    ms_local = e0.elapsed_time(e1)
-    value, ms = whole_job(ms_local, w.T, K, world)
-    assert B.moe_last_device_error(stream) == 0
-
-    result = None
-    if rank == 0:
-        # the dispatched rows and expert offsets of this batch, through the
-        # route and permute calls (the routing statistics come from the GPU path)
-        ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
-        tw = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
-        rb = B.moe_route_workspace_bytes(w.T, w.H, w.E)
-        pb = B.moe_permute_workspace_bytes(w.T, w.E)
-        rws = torch.empty(max(rb, pb, 256), dtype=torch.uint8, device=dev)
-        offs = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
-        st = torch.empty(w.T * w.k, dtype=torch.int32, device=dev)
-        inv = torch.empty(w.T * w.k, dtype=torch.int32, device=dev)
-        xperm = torch.empty((w.T * w.k, w.H), dtype=torch.bfloat16, device=dev)
-        B.moe_route(x, base.tensors[0], base.tensors[1], w.T, w.H, w.E, w.k, ids, tw, rws, rb, stream)
-        B.moe_permute(ids, x, w.T, w.H, w.E, w.k, offs, st, inv, xperm, rws, pb, stream)
         stream.synchronize()
-        nonempty = int((offs[1:] - offs[:-1] > 0).sum().item())
-        lbytes, lflops = layer_units(w, nonempty)
-        pk, pk_src = peaks()
-        step_s = ms / 1e3 / K
-        hbm = pk["hbm_gbs"] * 1e9
-        tc = pk["bf16_tflops_sustained"] * 1e12
-        t_roof = max(lbytes / hbm, lflops / tc)
-        layer_roof = {"bytes": lbytes, "flops": lflops, "nonempty_experts": nonempty,
-                      "roofline_us": t_roof * 1e6, "step_us": step_s * 1e6, "frac": t_roof / step_s,
-                      "bound": "hbm" if lbytes / hbm >= lflops / tc else "tensor",
-                      "peaks": f"{pk_src}: {pk['hbm_gbs']} GB/s, {pk['bf16_tflops_sustained']} TFLOP/s sustained"}
+        if K is None:                           # sweep: about SWEEP_SECONDS of replays
+            ms, _, _ = _timed_graph(graphs, stream, 2 * R, e0, e1)
+            K = int(min(20000, max(20, SWEEP_SECONDS * 1e3 / max(ms / (2 * R), 1e-3))))
+        torch.cuda.synchronize()
+        ms, t0, t1 = _timed_graph(graphs, stream, K, e0, e1, pre_s=0.15 if headline else 0.0,
+                                  post_s=0.1 if headline else 0.0)
+    torch.cuda.synchronize()
+    clocks = clk.window(t0, t1, pad=0.03)
+    assert B.moe_last_device_error(stream) == 0
+    value = tokens_per_s(w.T, K, ms)
 
-        # dominant kernel: the routed gate_up GroupedMatmul, timed alone on the
-        # layer's own dispatched rows, back to back in one graph over the weight copies
-        h = torch.empty((w.T * w.k, w.I), dtype=torch.bfloat16, device=dev)
-        gb_ws = B.moe_grouped_gemm_workspace_bytes(w.E, w.T * w.k, w.I, w.H, 1)
-        g_ws = torch.zeros(max(gb_ws, 256), dtype=torch.uint8, device=dev)
-        M = max(20, min(400, K))
+    # the routing of this batch, through the route and permute calls
+    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    tw = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    rb = B.moe_route_workspace_bytes(w.T, w.H, w.E)
+    pb = B.moe_permute_workspace_bytes(w.T, w.E)
+    rws = torch.empty(max(rb, pb, 256), dtype=torch.uint8, device=dev)
+    offs = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    st = torch.empty(w.T * w.k, dtype=torch.int32, device=dev)
+    inv = torch.empty(w.T * w.k, dtype=torch.int32, device=dev)
+    xperm = torch.empty((w.T * w.k, w.H), dtype=torch.bfloat16, device=dev)
+    B.moe_route(x, wr, b, w.T, w.H, w.E, w.k, ids, tw, rws, rb, stream)
+    B.moe_permute(ids, x, w.T, w.H, w.E, w.k, offs, st, inv, xperm, rws, pb, stream)
+    stream.synchronize()
+    nonempty = int((offs[1:] - offs[:-1] > 0).sum().item())
+    pk, pk_src = peaks()
+    lbytes, lflops = layer_units(w, nonempty)
+    step_s = ms / 1e3 / K
+    hbm = pk["hbm_gbs"] * 1e9
+    tc = pk["bf16_tflops_sustained"] * 1e12
+    t_roof = max(lbytes / hbm, lflops / tc)
+    layer_roof = {"bytes": lbytes, "flops": lflops, "nonempty_experts": nonempty,
+                  "roofline_us": t_roof * 1e6, "step_us": step_s * 1e6, "frac": t_roof / step_s,
+                  "bound": "hbm" if lbytes / hbm >= lflops / tc else "tensor",
+                  "peaks": f"{pk_src}: {pk['hbm_gbs']} GB/s, {pk['bf16_tflops_sustained']} TFLOP/s sustained"}
+    roof = dominant_kernel(w, copies, wr, b, x, offs, xperm, nonempty, pk, pk_src, stream, e0, e1, K)
+    res = {"value": value, "ms_per_step": ms / K, "steps": K, "warmup": W, "layer_roofline": layer_roof,
+           "roofline": roof, "clocks": clocks, "launches_per_step": launches, "graph_matches_eager": graph_same,
+           "config": config_of(w)}
+    if headline:
+        res["e2e"] = end_to_end(w, layers, outs, x, stream, e0, e1, K)
+    del graphs
+    return res
+
+
+def dominant_kernel(w, copies, wr, b, x, offs, xperm, nonempty, pk, pk_src, stream, e0, e1, K):
+    """The step's dominant work, timed alone back to back in one graph over the
+    weight copies, in the configuration the layer itself runs.  Up to 16
+    tokens: the routed path (the layer without its shared expert: router and
+    dispatch, gate_up reading the dispatched rows of x through the sort, down,
+    combine).  Above: the routed gate_up GroupedMatmul on the layer's
+    dispatched rows."""
+    import torch
+
+    from moe_ffn_layer_gb300 import binding as B
+    from moe_ffn_layer_gb300.layer import MoEFFN
+    R = len(copies)
+    M = max(20, min(400, K))
+    if w.T <= 16:
+        routed = [MoEFFN(w.k, wr, b, c[0], c[1], None, None) for c in copies]
+        o = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=x.device)
+        for L in routed:
+            L.forward(x, o, stream)
+        n_launch = None
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             cs = torch.cuda.current_stream()
             for i in range(M):
-                B.moe_grouped_gemm(xperm, layers[i % R].tensors[2], offs, w.E, w.T * w.k, w.I, w.H, 1, h, g_ws,
-                                   gb_ws, cs)
-        with torch.cuda.stream(stream):
-            g.replay()
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-        e1.synchronize()
-        assert B.moe_last_device_error(stream) == 0
-        k_us = e0.elapsed_time(e1) * 1e3 / M
+                routed[i % R].forward(x, o, cs)
+                n_launch = B.moe_last_launch_count()
+        kernel = "routed path (layer without its shared expert)"
+        gb, gf = routed_units(w, nonempty)
+    else:
+        h = torch.empty((w.T * w.k, w.I), dtype=torch.bfloat16, device=x.device)
+        gb_ws = B.moe_grouped_gemm_workspace_bytes(w.E, w.T * w.k, w.I, w.H, 1)
+        g_ws = torch.zeros(max(gb_ws, 256), dtype=torch.uint8, device=x.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            cs = torch.cuda.current_stream()
+            for i in range(M):
+                B.moe_grouped_gemm(xperm, copies[i % R][0], offs, w.E, w.T * w.k, w.I, w.H, 1, h, g_ws, gb_ws, cs)
+                n_launch = B.moe_last_launch_count()
+        kernel = "grouped_gemm gate_up+SiLU*mul"
         gb, gf = gate_up_units(w, nonempty)
-        if w.T * w.k <= 64 * w.E:     # weights-on-M form: weight streaming, HBM-bound
-            achieved = gb / (k_us * 1e-6) / 1e9
-            roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / pk["hbm_gbs"]}
-        else:
-            achieved = gf / (k_us * 1e-6) / 1e12
-            roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": achieved / pk["bf16_tflops"]}
-        roof.update({"traffic": _traffic(w), "kernel": "grouped_gemm gate_up+SiLU*mul", "us_per_launch": k_us,
-                     "algorithmic_bytes": gb, "algorithmic_flops": gf, "peak_source": pk_src + " (burst)"})
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    assert B.moe_last_device_error(stream) == 0
+    k_us = e0.elapsed_time(e1) * 1e3 / M
+    if w.T * w.k <= 64 * w.E:     # weight streaming: HBM-bound
+        achieved = gb / (k_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"]}
+    else:
+        achieved = gf / (k_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"]}
+    roof.update({"traffic": _traffic(w), "kernel": kernel, "us_per_launch": k_us, "launches": n_launch,
+                 "algorithmic_bytes": gb, "algorithmic_flops": gf, "peak_source": pk_src + " (burst)"})
+    return roof
 
-        # end to end through the public call: pinned host x -> device, forward, out -> pinned host
-        xh = x.cpu().pin_memory()
-        oh = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-        xd = torch.empty_like(x)
-        KE = max(5, min(K, 200))
-        with torch.cuda.stream(stream):
-            for i in range(3):
-                xd.copy_(xh, non_blocking=True)
-                layers[i % R].forward(xd, outs[i % R], stream)
-                oh.copy_(outs[i % R], non_blocking=True)
-            stream.synchronize()
-            e0.record(stream)
-            for i in range(KE):
-                xd.copy_(xh, non_blocking=True)
-                layers[i % R].forward(xd, outs[i % R], stream)
-                oh.copy_(outs[i % R], non_blocking=True)
-            e1.record(stream)
-        e1.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / KE
-        e2e = {"value": w.T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": w.T * w.H * 2,
-               "d2h_bytes_per_step": w.T * w.H * 2, "ms_per_step": e2e_ms,
-               "path": "MoEFFN.forward (one moe_forward call), no graph"}
 
+def end_to_end(w, layers, outs, x, stream, e0, e1, K):
+    """The same metric through the public call: pinned host x -> device,
+    forward, out -> pinned host, every step, no graph."""
+    import torch
+    R = len(layers)
+    xh = x.cpu().pin_memory()
+    oh = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    KE = max(5, min(K, 200))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            xd.copy_(xh, non_blocking=True)
+            layers[i % R].forward(xd, outs[i % R], stream)
+            oh.copy_(outs[i % R], non_blocking=True)
+        stream.synchronize()
+        e0.record(stream)
+        for i in range(KE):
+            xd.copy_(xh, non_blocking=True)
+            layers[i % R].forward(xd, outs[i % R], stream)
+            oh.copy_(outs[i % R], non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / KE
+    return {"value": w.T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": w.T * w.H * 2,
+            "d2h_bytes_per_step": w.T * w.H * 2, "ms_per_step": e2e_ms, "steps": KE,
+            "path": "MoEFFN.forward (one moe_forward call), no graph"}
+
+
+def run_gpu(args, w):
+    import torch
+
+    from moe_ffn_layer_gb300 import build as build_mod
+    from moe_ffn_layer_gb300 import synth
+
+    build_mod.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    clk = ClockSampler(0)
+    beds = {}
+
+    def bed_for(wl):
+        key = (wl.H, wl.E, wl.I, wl.Is, wl.sigma_w)
+        if key not in beds:
+            if len(beds) >= 1:          # one set of weights on the device at a time
+                beds.clear()
+                torch.cuda.empty_cache()
+            beds[key] = WeightBed(wl, args.seed, dev)
+        return beds[key]
+
+    try:
+        head = measure(w, bed_for(w), args, clk, args.steps, args.warmup, headline=True)
         cpu = None
         if not args.no_cpu_baseline:
+            inp = dict(zip(("x", "w_router", "bias"), synth.make_activations(w, args.seed)))
+            inp.update(bed_for(w).host)
             tps, cores, ntok, el = time_oracle(w, inp, args.cpu_budget)
             cpu = {"value": tps, "unit": UNIT, "cores": round(cores, 2), "kind": "oracle",
                    "sample": f"{ntok} tokens of the same workload through the float64 oracle, token batches "
-                             f"of {min(w.T, 8) if w.T > 16 else w.T}, {el:.1f} s wall; cores = CPU time / wall time "
-                             f"(numpy BLAS pool of {os.cpu_count()} threads)"}
+                             f"of {min(w.T, 8) if w.T > 16 else w.T}, {el:.1f} s wall; cores = CPU time / wall "
+                             f"time (numpy BLAS pool of {os.cpu_count()} threads)"}
+        sweep = {}
+        if not args.no_sweep:
+            for name, T in SWEEP:
+                wl = synth.workload(name, T)
+                r = measure(wl, bed_for(wl), args, clk, None, 5)
+                sweep[r["config"]["workload"]] = {k: r[k] for k in ("value", "ms_per_step", "steps", "layer_roofline",
+                                                                    "roofline", "clocks", "launches_per_step",
+                                                                    "graph_matches_eager")}
+    finally:
+        clk.stop()
 
-        result = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
-            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic (seeded; workload shapes and distributions)",
-            "config": {"workload": f"{w.name.split('@')[0]} T={w.T}", "T": w.T, "H": w.H, "E": w.E, "k": w.k,
-                       "I": w.I, "I_s": w.Is, "routing": _routing_desc(w), "parallelism": f"replicas x{world}",
-                       "l2": f"expert weights rotate over {R} device copies ({R} x {touched / 1e6:.0f} MB touched "
-                             f">= 4 x L2); one CUDA graph per copy, replayed back to back"},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": K * launches, "launches_per_step": launches,
-            "roofline": roof, "layer_roofline": layer_roof, "cpu_baseline": cpu,
-        }
-    barrier(world)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    result = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; workload shapes and distributions)",
+        "config": head["config"], "clocks": head["clocks"], "e2e": head["e2e"],
+        "gpu_launches": args.steps * head["launches_per_step"], "launches_per_step": head["launches_per_step"],
+        "roofline": head["roofline"], "layer_roofline": head["layer_roofline"], "cpu_baseline": cpu,
+        "graph_matches_eager": head["graph_matches_eager"],
+        "clocks_note": "sampled every 20 ms; the headline window spans 0.15 s of untimed replays of the same "
+                       "graphs before the timed steps and 0.1 s after them",
+    }
+    if sweep:
+        result["workloads"] = sweep
     return result
-
-
-def _routing_desc(w):
-    if w.zipf_s is None and not w.n_empty:
-        return f"router W ~ N(0,{w.sigma_router}), near-uniform"
-    s = f"router W ~ N(0,{w.sigma_router}) + Zipf(s={w.zipf_s}) log-rank bias"
-    return s + (f", {w.n_empty} experts forced empty" if w.n_empty else "")
-
-
-def _traffic(w):
-    """DRAM bytes per launch of the dominant kernel from a committed ncu
-    capture of the same kernel source, else None."""
-    import hashlib
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
-        return None
-    src = os.path.join(ROOT, "moe_ffn_layer_gb300", "csrc", "grouped_gemm.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    d = json.load(open(p))
-    e = d.get(f"{w.name.split('@')[0]}@T{w.T}")
-    if not e or e.get("source_sha") != h:
-        return None
-    return e.get("dram_bytes_per_launch")
 
 
 # ---------------------------------------------------------------- reference arm
@@ -404,12 +522,41 @@ def run_reference(args, w):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded; workload shapes and distributions)",
-            "config": {"workload": f"{w.name.split('@')[0]} T={w.T}", "T": w.T, "H": w.H, "E": w.E, "k": w.k,
-                       "I": w.I, "I_s": w.Is, "routing": _routing_desc(w)},
+            "data": "synthetic (seeded; workload shapes and distributions)", "config": config_of(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": round(cores, 2), "kind": "oracle",
                              "sample": f"{n} random tokens of the workload per step through the float64 oracle"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _traffic(w):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    capture of the same kernel source, else None."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(f"{w.name.split('@')[0]}@T{w.T}")
+    if not e:
+        return None
+    src = os.path.join(ROOT, "moe_ffn_layer_gb300", "csrc", e.get("source", "grouped_gemm.cu"))
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if e.get("source_sha") != h:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def refuse_multi_gpu(args) -> bool:
+    """True (after printing one line) when asked for more than one GPU."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus <= 1 and world <= 1:
+        return False
+    if int(os.environ.get("RANK", "0")) == 0:
+        print(json.dumps({"metric": METRIC, "unit": UNIT, "n_gpus": max(args.gpus, world), "impl": args.impl,
+                          "unavailable": f"multi-GPU runs closed on this pool; {ONE_GPU}"}), flush=True)
+    return True
 
 
 def main():
@@ -423,13 +570,16 @@ def main():
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="time the named workload only")
     ap.add_argument("--copies", type=int, default=0, help="weight copies to rotate over (0: enough to defeat L2)")
     args = ap.parse_args()
+    if args.impl == "own" and refuse_multi_gpu(args):
+        return
     from moe_ffn_layer_gb300 import synth
     T = args.T if args.T is not None else (8 if args.workload == "decode" else None)
     w = synth.workload(args.workload, T)
     if args.steps is None:
-        args.steps = DEFAULT_STEPS[args.workload] if args.impl == "own" else 20
+        args.steps = 200 if args.impl == "own" else 20
     args.warmup = max(args.warmup, 3)
     res = run_reference(args, w) if args.impl == "reference" else run_gpu(args, w)
     if res is not None:

@@ -22,7 +22,14 @@
  *
  * Conventions for every call:
  *  - Pointers are DEVICE pointers unless stated otherwise; the caller owns all
- *    memory, streams and events.  No call allocates device memory.
+ *    memory, streams and events.  No call allocates device memory.  The
+ *    matmul operands (a, w and out of the grouped matmul; x, out, the
+ *    workspace and the expert weights of the layer forward) must be device
+ *    memory of the current device (cudaMalloc-type memory, not host, managed
+ *    or another GPU's memory): the kernels read them with TMA, some of it
+ *    multicast between the two CTAs of a cluster of this GPU.  Other
+ *    pointers are refused with MOE_ERR_UNSUPPORTED before any launch.  The
+ *    library runs on one GPU: it makes no peer access and no collective.
  *  - Every call is asynchronous on the given stream and never synchronises
  *    with the host (moe_last_device_error excepted).
  *  - bf16 tensors are row-major, 16-byte aligned; K-major weights ([rows][K]).
@@ -156,8 +163,10 @@ MOE_API int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_
  *  - Allocates nothing: no cudaMalloc or cudaFree, no allocating library call.
  *    It clears the scratch counters with cudaMemsetAsync on `stream`.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress with that device current); make that first call
- *    before any stream capture on the device.
+ *    (cudaGetSymbolAddress with that device current) and keeps it for that
+ *    device's current context; make that first call before any stream
+ *    capture on the device.  A call in a new context (after cudaDeviceReset,
+ *    say) looks the address up again, so again call it once before capturing.
  *  - Every call uses the same array and it keeps the previous call's data:
  *    calls that overlap on the GPU (other streams, other threads) race on it
  *    and give wrong results.  Order them on one stream.
@@ -202,6 +211,30 @@ MOE_API int moe_last_device_error(cudaStream_t stream);
 /* Number of kernels the last successful call of each entry point launched on
  * the current host thread (for accounting in benchmarks). */
 MOE_API int moe_last_launch_count(void);
+
+/* Where moe_forward keeps the routing and the dispatch of a batch inside its
+ * workspace: byte offsets from the start of ws, for a layer of sizes d and a
+ * batch of T tokens.  After a moe_forward call on that workspace has
+ * completed, the regions hold that call's
+ *   topk_ids int32 [T][k], topk_w fp32 [T][k] (as moe_route returns them),
+ *   expert_offsets int32 [E+1], sorted_token int32 [T*k], inv_perm int32 [T*k]
+ *   (as moe_permute returns them),
+ * so that a caller can inspect the layer's own expert choice and dispatch.
+ * Returns MOE_ERR_INVALID / MOE_ERR_UNSUPPORTED as moe_workspace_bytes
+ * refuses the sizes. */
+typedef struct {
+  size_t topk_ids, topk_w, expert_offsets, sorted_token, inv_perm;
+} moe_workspace_offsets;
+MOE_API int moe_workspace_layout(const moe_dims* d, int T, moe_workspace_offsets* out);
+
+/* Limit, in nanoseconds, of the device-side bounded waits of kernels launched
+ * from now on by any host thread (default 2e9; waits that drain copies
+ * already in flight keep the default).  A wait that reaches it records
+ * MOE_ERR_TIMEOUT, the kernel abandons its work and exits.  0 makes every
+ * wait that is not already complete at its first test expire at once: for
+ * tests of the timeout path only (outputs are then not written).  Launches
+ * captured in a CUDA graph keep the limit of the capture. */
+MOE_API int moe_debug_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -29,6 +29,11 @@ class moe_dims(ctypes.Structure):
                 ("I_s", ctypes.c_int)]
 
 
+class moe_workspace_offsets(ctypes.Structure):
+    _fields_ = [("topk_ids", ctypes.c_size_t), ("topk_w", ctypes.c_size_t), ("expert_offsets", ctypes.c_size_t),
+                ("sorted_token", ctypes.c_size_t), ("inv_perm", ctypes.c_size_t)]
+
+
 class moe_weights(ctypes.Structure):
     _fields_ = [("w_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p),
                 ("w_down", ctypes.c_void_p), ("ws_gate_up", ctypes.c_void_p), ("ws_down", ctypes.c_void_p)]
@@ -49,6 +54,8 @@ _SIGS = {
                          _P]),
     "moe_last_device_error": (_I, [_P]),
     "moe_last_launch_count": (_I, []),
+    "moe_workspace_layout": (_I, [ctypes.POINTER(moe_dims), _I, ctypes.POINTER(moe_workspace_offsets)]),
+    "moe_debug_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
 }
 
 _lib = None
@@ -160,3 +167,13 @@ def moe_last_device_error(stream) -> int:
 
 def moe_last_launch_count() -> int:
     return lib().moe_last_launch_count()
+
+
+def moe_workspace_layout(dims: moe_dims, T: int) -> moe_workspace_offsets:
+    out = moe_workspace_offsets()
+    _check("moe_workspace_layout", lib().moe_workspace_layout(ctypes.byref(dims), T, ctypes.byref(out)))
+    return out
+
+
+def moe_debug_set_wait_limit_ns(ns: int) -> int:
+    return _check("moe_debug_set_wait_limit_ns", lib().moe_debug_set_wait_limit_ns(ns))

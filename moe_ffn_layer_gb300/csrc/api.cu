@@ -10,6 +10,7 @@
 // preallocates events instead of creating them per step: here the caller owns
 // exactly two events and the library creates none.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -34,9 +35,12 @@ int fork_stage(const moe_dims* d, int T) {
   return static_cast<double>(T) * d->E * d->H >= 8589934592.0 ? 0 : 1;
 }
 
+std::atomic<uint64_t> g_wait_limit_ns{moe::kWaitTimeoutNs};
+
 struct DevInfo {
   int* status = nullptr;
   int sms = 0;
+  void* ctx = nullptr;   // the context the status address belongs to
   bool init = false;
 };
 constexpr int kMaxDevices = 64;
@@ -47,13 +51,19 @@ int dev_info(DevInfo** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  void* ctx = nullptr;
+  if (moe::current_context(&ctx) != MOE_OK) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   DevInfo& d = g_dev[dev];
-  if (!d.init) {
+  // the status word's address is looked up once per context (a device reset
+  // makes a new context, which holds its own copy of the word)
+  if (!d.init || d.ctx != ctx || !ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!ctx && moe::current_context(&ctx) != MOE_OK) return MOE_ERR_CUDA;   // set up by the lookup
     d.status = static_cast<int*>(p);
+    d.ctx = ctx;
     d.init = true;
   }
   *out = &d;
@@ -126,6 +136,41 @@ int check_dims(const moe_dims* d) {
 }  // namespace
 
 namespace moe {
+
+void set_last_launches(int n) { t_last_launches = n; }
+
+int current_context(void** ctx) {
+  using GetCtxFn = CUresult (*)(CUcontext*);
+  static GetCtxFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<GetCtxFn>(p);
+  });
+  if (!fn) return MOE_ERR_CUDA;
+  CUcontext c = nullptr;   // null until the runtime has set up the device
+  if (fn(&c) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  *ctx = c;
+  return MOE_OK;
+}
+
+bool device_local(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();   // a pointer the runtime does not know: clear the error the query left
+    return false;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 int current_device_info(int** status, int* num_sms) {
   DevInfo* di = nullptr;
   const int rc = dev_info(&di);
@@ -214,6 +259,8 @@ int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets,
   if (!al16(a) || !al16(w) || !al16(out) || (reinterpret_cast<uintptr_t>(group_offsets) & 3u) ||
       (reinterpret_cast<uintptr_t>(ws) & 255u))
     return MOE_ERR_UNSUPPORTED;
+  // TMA reads the operands: device memory of the current GPU only
+  if (!moe::device_local(a) || !moe::device_local(w) || !moe::device_local(out)) return MOE_ERR_UNSUPPORTED;
   DevInfo* di = nullptr;
   int rc = dev_info(&di);
   if (rc) return rc;
@@ -263,6 +310,11 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
     return MOE_ERR_UNSUPPORTED;
   const Layout L = layout(d, T);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  // the matmuls read x, the weights and the workspace by TMA: device memory of the current GPU only
+  if (!moe::device_local(x) || !moe::device_local(out) || !moe::device_local(ws) ||
+      !moe::device_local(w->w_gate_up) || !moe::device_local(w->w_down) ||
+      (has_shared && (!moe::device_local(w->ws_gate_up) || !moe::device_local(w->ws_down))))
+    return MOE_ERR_UNSUPPORTED;
   DevInfo* di = nullptr;
   rc = dev_info(&di);
   if (rc) return rc;
@@ -375,5 +427,23 @@ int moe_last_device_error(cudaStream_t stream) {
 }
 
 int moe_last_launch_count(void) { return t_last_launches; }
+
+int moe_workspace_layout(const moe_dims* d, int T, moe_workspace_offsets* out) {
+  if (!out || T < 0) return MOE_ERR_INVALID;
+  const int rc = check_dims(d);
+  if (rc) return rc;
+  const Layout L = layout(d, T);
+  out->topk_ids = L.ids;
+  out->topk_w = L.w;
+  out->expert_offsets = L.offsets;
+  out->sorted_token = L.sorted;
+  out->inv_perm = L.inv;
+  return MOE_OK;
+}
+
+int moe_debug_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+  return MOE_OK;
+}
 
 }  // extern "C"

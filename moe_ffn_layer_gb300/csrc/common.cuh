@@ -18,7 +18,8 @@ constexpr int kMaxTopK = 16;       // k supported by the router
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a = 256) { return (v + a - 1) / a * a; }
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer and
-// records MOE_ERR_TIMEOUT in the device status word.
+// records MOE_ERR_TIMEOUT in the device status word (the default of the
+// limit that launches carry; waits that drain copies in flight always use it).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
 __device__ __forceinline__ void set_status(int* status, int code) {
@@ -118,18 +119,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase of parity `parity` has completed.  Gives up (returns
 // false) when `abort` is raised by another role of the CTA or when the wait
-// exceeds kWaitTimeoutNs, in which case it records MOE_ERR_TIMEOUT and raises
-// `abort` itself.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+// exceeds `limit_ns` of %globaltimer, in which case it records MOE_ERR_TIMEOUT
+// and raises `abort` itself.  limit_ns == 0 (tests of the timeout path): a
+// phase that is not complete at the first, non-blocking test expires at once.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                          uint64_t limit_ns) {
+  if (limit_ns == 0) {
+    if (mbar_test_wait(bar, parity)) return true;
+    set_status(status, MOE_ERR_TIMEOUT);
+    *abort = 1;
+    return false;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (globaltimer() - t0 > limit_ns) {
         set_status(status, MOE_ERR_TIMEOUT);
         *abort = 1;
         return false;

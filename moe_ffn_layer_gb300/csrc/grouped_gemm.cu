@@ -46,6 +46,8 @@
 // last adds the pieces' partials in piece order, resets the counter to zero
 // and runs the epilogue.  The result does not depend on which CTA arrives
 // last, and no CTA waits for another.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -109,6 +111,7 @@ struct GemmArgs {
                            // run of them along B's K (tokens-on-M form only)
   const int32_t* a_rows;   // non-null: token row r is row a_rows[r] of the token tensor
                            // (fetched with TMA gather4; no permuted copy needed)
+  uint64_t wait_ns;        // limit of every bounded wait but the drains (0: expire at once)
 };
 
 // fp32 values one TMEM lane keeps per split-K partial
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       if (lane == 0) {
         for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status)) { ok = false; break; }
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
           uint8_t* sa = stage_base + stage * C::kStageBytes;
           uint8_t* sb = sa + C::kABytes;
           const int kc = kb * kBK;
@@ -474,13 +477,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           idesc = idesc_bf16_f32(128, W);
         }
-        if (!mbar_wait(&tempty_bar[ab], aphase ^ 1u, abort_flag, args.status)) break;
+        if (!mbar_wait(&tempty_bar[ab], aphase ^ 1u, abort_flag, args.status, args.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * C::kAccCols;
         const int kb0 = pc.kb0;
         bool ok = true;
         for (int kb = kb0; kb < pc.kb1; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag, args.status)) { ok = false; break; }
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * C::kStageBytes);
           const uint32_t sb = sa + C::kABytes;
@@ -529,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = pc.u;
       int g, row0, nrows, wb, kind;
       decode(u, g, row0, nrows, wb, kind);
-      bool ok = mbar_wait(&tfull_bar[ab], aphase, abort_flag, args.status);
+      // the warp leaves together or not at all (tcgen05.ld below is warp-wide)
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[ab], aphase, abort_flag, args.status, args.wait_ns));
       if (P > 1) {
         // the split path meets at named barriers: the four warps leave together or not at all
         if (lane == 0) s_split[2 + q] = ok ? 1 : 0;
@@ -794,10 +798,13 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
                int max_slots = kMaxSlots, int K_a = 0, const int32_t* a_rows = nullptr, int a_src_rows = 0) {
   using C = Cfg<SWAP, W, ACT, MC>;
   auto kernel = grouped_gemm_kernel<SWAP, W, ACT, MC>;
+  // per device: the shared-memory attribute set once, the pairs that fit at once
   static bool attr_done[64] = {};
   static int max_clusters[64] = {};
+  static std::mutex mu;
   int dev = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  std::unique_lock<std::mutex> lk(mu);
   if (dev >= 64 || !attr_done[dev]) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -822,6 +829,8 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
       attr_done[dev] = true;
     }
   }
+  const int mc = dev < 64 ? max_clusters[dev] : 1;
+  lk.unlock();
   CUtensorMap tt, tw;
   const int wrows = ACT == 1 ? 2 * N : N;
   const uint32_t tok_box = SWAP ? 16 : (MC ? 64 : 128);
@@ -837,7 +846,7 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   long long bound = (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) *
                     (N / C::kOutCols / (MC ? 2 : 1));
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
-                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows};
+                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows, wait_limit_ns()};
   if (SWAP && scratch && scratch->counters && scratch->partials) {
     const SplitPlan p = split_plan(G, rows_max, N, ACT, max_slots);
     if (p.partial_bytes && scratch->partial_bytes >= p.partial_bytes) {
@@ -851,7 +860,6 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   if (MC) {
     // one work list per pair: at most grid_cap / 2 pairs, and no more than fit at once
     long long pairs = grid_cap / 2;
-    const int mc = dev < 64 ? max_clusters[dev] : 1;
     if (pairs > mc) pairs = mc;
     if (pairs > bound) pairs = bound;
     if (pairs < 1) pairs = 1;
@@ -922,6 +930,10 @@ int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, in
     return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,
                                        launches, max_slots, 0, a_rows, a_src_rows);
   }
+  // the pairs multicast operand tiles inside a cluster of this GPU: only for
+  // operands in this GPU's own device memory
+  const bool pairs_ok = kPairs && !a_rows && grid_cap >= 2 && (N % 256 == 0 || N % 512 == 0);
+  if (pairs_ok && (!device_local(a) || !device_local(w))) return MOE_ERR_UNSUPPORTED;
   if (act == 1) {
     if (N % 256 == 0 && kPairs && !a_rows && grid_cap >= 2)
       return launch_cfg<0, 256, 1, 1>(a, w, offsets, G, rows_max, N, K, out, status, nullptr, grid_cap, stream,

@@ -84,4 +84,18 @@ int combine_launch(const void* y, const int32_t* inv_perm, const float* topk_w, 
 // Status word and SM count of the current device (first use looks them up).
 int current_device_info(int** status, int* num_sms);
 
+// What moe_last_launch_count() reports on this host thread.
+void set_last_launches(int n);
+
+// The calling thread's current CUDA context (null before the runtime has set
+// up the current device).
+int current_context(void** ctx);
+
+// True when p is device memory (cudaMemoryTypeDevice) of the current device.
+bool device_local(const void* p);
+
+// Limit of the kernels' bounded waits for launches made from now on
+// (kWaitTimeoutNs unless a test lowered it).
+uint64_t wait_limit_ns();
+
 }  // namespace moe

@@ -61,6 +61,29 @@ def test_workspace_queries(lib):
     assert B.moe_grouped_gemm_workspace_bytes(128, 64, 768, 2048, 1) >= 128 * 64 * 4
 
 
+def test_workspace_layout(lib):
+    """The regions where the layer forward leaves its routing and dispatch lie
+    inside its workspace, 256-byte aligned, large enough and disjoint."""
+    for dims, T in [(B.moe_dims(2048, 128, 8, 768, 2048), 8), (B.moe_dims(256, 8, 2, 128, 256), 16),
+                    (B.moe_dims(2048, 128, 8, 768, 2048), 8192), (B.moe_dims(256, 8, 2, 128, 0), 1)]:
+        total = B.moe_workspace_bytes(dims, T)
+        o = B.moe_workspace_layout(dims, T)
+        Tk = T * dims.k
+        regions = sorted([(o.topk_ids, Tk * 4), (o.topk_w, Tk * 4), (o.expert_offsets, (dims.E + 1) * 4),
+                          (o.sorted_token, Tk * 4), (o.inv_perm, Tk * 4)])
+        for (a, n), (b, _) in zip(regions, regions[1:]):
+            assert a + n <= b
+        for a, n in regions:
+            assert a % 256 == 0 and a + n <= total
+    assert _rc(B.moe_workspace_layout, B.moe_dims(2048, 128, 8, 700, 2048), 8) == -2
+    assert _rc(B.moe_workspace_layout, B.moe_dims(2048, 128, 8, 768, 2048), -1) == -1
+
+
+def test_wait_limit_setter_needs_no_device(lib):
+    assert B.moe_debug_set_wait_limit_ns(0) == 0
+    assert B.moe_debug_set_wait_limit_ns(2_000_000_000) == 0
+
+
 def _rc(fn, *args):
     with pytest.raises(B.MoEError) as e:
         fn(*args)

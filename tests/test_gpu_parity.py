@@ -21,7 +21,9 @@ from oracle import moe_oracle as om
 pytestmark = pytest.mark.gpu
 
 SMALL_SHAPES = [s for s in synth.FULL_SHAPES if s[1] <= 256]
-LARGE_SHAPES = [s for s in synth.FULL_SHAPES if s[1] > 256]
+# prefill T=8192: the whole output against the oracle; large prefill: sampled rows
+FULL_OUTPUT_SHAPES = SMALL_SHAPES + [("prefill", 8192)]
+LARGE_SHAPES = [s for s in synth.FULL_SHAPES if s[1] > 8192]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -358,8 +360,11 @@ def test_combine(name, T):
 
 # ---------------------------------------------------------------- whole layer
 
-@pytest.mark.parametrize("name,T", SMALL_SHAPES)
+@pytest.mark.parametrize("name,T", FULL_OUTPUT_SHAPES)
 def test_forward_full(name, T):
+    """Every output element of the layer against the float64 oracle (at
+    prefill T=8192 the tokens-on-M matmuls run as CTA pairs, both pair modes:
+    groups with an even and with an odd number of 128-row tiles)."""
     w = synth.workload(name, T)
     inp = inputs(name, T)
     ref = om.forward(inp, w.k)
@@ -379,14 +384,24 @@ def _sample_tokens(name, T, n=24):
     g0, g1 = int(off[hot]), int(off[hot + 1])
     for r in (g0, g1 - 1, min(g0 + 127, g1 - 1), min(g0 + 128, g1 - 1)):
         pick.add(int(st[r]))
+    # groups whose last 128-row tile is odd (the pair shares that tile between two
+    # weight blocks) and groups with an even tile count: first and last row of the last tile
+    tiles = (counts + 127) // 128
+    for parity in (1, 0):
+        gs = [g for g in np.nonzero((tiles % 2 == parity) & (counts > 0))[0]]
+        for g in gs[:6]:
+            r0 = int(off[g]) + 128 * (int(tiles[g]) - 1)
+            pick.add(int(st[r0]))
+            pick.add(int(st[int(off[g + 1]) - 1]))
     return np.array(sorted(pick))
 
 
 @pytest.mark.parametrize("name,T", LARGE_SHAPES)
 def test_forward_sampled_full_size(name, T):
-    """Full-size prefill layers: every output is finite, and sampled rows
-    (random tokens plus tokens at the hot group's tile boundaries) match the
-    oracle evaluated token by token."""
+    """The large prefill layer: every output is finite, and sampled rows
+    (random tokens, tokens at the hot group's tile boundaries, and the first
+    and last rows of the last tile of groups with an odd and an even number of
+    tiles) match the oracle evaluated token by token."""
     w = synth.workload(name, T)
     inp = inputs(name, T)
     ids, wts, *_ = routing(name, T)
@@ -549,6 +564,92 @@ def test_forward_one_token_matches_standalone_calls(case):
     B.moe_unpermute_combine(y, inv, tw, sh, 1, H, k, out2, stream())
     no_device_error()
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+DISPATCH_CASES = [("decode", 1), ("decode", 4), ("decode", 8), ("tiny", 16), ("batched_decode", 64)]
+
+
+@pytest.mark.parametrize("name,T", DISPATCH_CASES)
+def test_forward_dispatch_bit_exact(name, T):
+    """The routing and dispatch the layer forward itself computed (read from
+    its workspace): expert ids, offsets, sorted tokens and the inverse
+    permutation bit-exact against the oracle, weights within the router
+    tolerance."""
+    w = synth.workload(name, T)
+    ids_ref, w_ref, off_ref, st_ref, inv_ref = routing(name, T)
+    L = layer(name, T)
+    ws = L.workspace(T)
+    ws.fill_(0)        # every region below must be written by this call
+    L.forward(x_tensor(name, T))
+    no_device_error()
+    o = B.moe_workspace_layout(L.dims, T)
+    Tk = T * w.k
+
+    def region(off, n, dtype):
+        return ws[off:off + n * 4].view(dtype).cpu().numpy()
+
+    np.testing.assert_array_equal(region(o.topk_ids, Tk, torch.int32).reshape(T, w.k), ids_ref)
+    np.testing.assert_allclose(region(o.topk_w, Tk, torch.float32).reshape(T, w.k), w_ref, rtol=0,
+                               atol=route_w_atol(T, w.H, w.E))
+    np.testing.assert_array_equal(region(o.expert_offsets, w.E + 1, torch.int32), off_ref)
+    np.testing.assert_array_equal(region(o.sorted_token, Tk, torch.int32), st_ref)
+    np.testing.assert_array_equal(region(o.inv_perm, Tk, torch.int32), inv_ref)
+    ws.fill_(0)        # leave the workspace as the layer expects it (counters zero)
+
+
+@pytest.mark.parametrize("name,T", [("decode", 1), ("decode", 8), ("batched_decode", 256), ("prefill", 8192)])
+def test_forward_graph_replay_matches_eager(name, T):
+    """The forward captured in a CUDA graph (as the benchmark times it) and
+    replayed gives the same bits as the eager call."""
+    L = layer(name, T)
+    x = x_tensor(name, T)
+    eager = L.forward(x).clone()
+    no_device_error()
+    s = torch.cuda.Stream()
+    out = torch.zeros_like(eager)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        L.forward(x, out, torch.cuda.current_stream())
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        no_device_error()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_operands_outside_device_memory_are_refused():
+    """The matmuls read their operands with TMA (the prefill form multicasts
+    them between the CTAs of a cluster): host memory, pinned or not, is refused
+    on the host before any launch."""
+    G, R, N, K = 2, 600, 512, 128          # tokens-on-M with 256-wide blocks: the pair form
+    w = torch.zeros((G, 2 * N, K), dtype=torch.bfloat16, device="cuda")
+    a = torch.zeros((R, K), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((R, N), dtype=torch.bfloat16, device="cuda")
+    offs = i32(np.array([0, 300, 600]))
+    B.moe_grouped_gemm(a, w, offs, G, R, N, K, 1, out, None, 0, stream())     # device memory: runs
+    no_device_error()
+    a_pinned = torch.zeros((R, K), dtype=torch.bfloat16).pin_memory()
+    a_host = np.zeros((R, K), dtype=np.uint16)
+    for bad in (a_pinned.data_ptr(), a_host.ctypes.data):
+        with pytest.raises(B.MoEError) as e:
+            B.moe_grouped_gemm(bad, w, offs, G, R, N, K, 1, out, None, 0, stream())
+        assert e.value.code == -2
+        with pytest.raises(B.MoEError) as e:
+            B.moe_grouped_gemm(a, bad, offs, G, R, N, K, 1, out, None, 0, stream())
+        assert e.value.code == -2
+        with pytest.raises(B.MoEError) as e:
+            B.moe_grouped_gemm_noalloc(bad, w, offs, G, R, N, K, 1, out, stream())
+        assert e.value.code == -2
+    # the layer forward: x in host memory
+    L = layer("tiny", 16)
+    x_pinned = torch.zeros((16, 256), dtype=torch.bfloat16).pin_memory()
+    ws = L.workspace(16)
+    o = torch.empty((16, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.MoEError) as e:
+        B.moe_forward(L.dims, L.weights, x_pinned, 16, o, ws, ws.numel(), stream(), L.side, L.ev_fork, L.ev_join)
+    assert e.value.code == -2
+    no_device_error()
 
 
 def test_forward_repeatable_and_launch_count():

@@ -1,7 +1,8 @@
 """moe_grouped_gemm_noalloc: the grouped matmul for callers that cannot
 allocate device memory (its split-K scratch is a fixed array inside the
 library).  Its output must match moe_grouped_gemm's on the same inputs, call
-after call, since every call reuses the same array.
+after call, since every call reuses the same array, and the float64 oracle
+within the layer's tolerance.
 
 This file is collected last on purpose, so that a run that stops at the first
 failure has already run every other test."""
@@ -14,6 +15,7 @@ from moe_ffn_layer_gb300 import binding as B
 from moe_ffn_layer_gb300 import build as build_mod
 from moe_ffn_layer_gb300 import synth
 from moe_ffn_layer_gb300.layer import bf16_tensor
+from oracle import moe_oracle as om
 
 pytestmark = pytest.mark.gpu
 
@@ -41,22 +43,28 @@ def test_noalloc_matches_grouped_gemm(rows, N, K, act):
     G = len(rows)
     off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
     R = int(off[-1])
-    a = bf16_tensor(synth.random_bf16((R, K), seed=R + K, tag=61), "cuda")
-    w = bf16_tensor(synth.random_bf16((G, 2 * N if act else N, K), seed=N + G, tag=62, sigma=0.03), "cuda")
+    a_bits = synth.random_bf16((R, K), seed=R + K, tag=61)
+    w_bits = synth.random_bf16((G, 2 * N if act else N, K), seed=N + G, tag=62, sigma=0.03)
+    a = bf16_tensor(a_bits, "cuda")
+    w = bf16_tensor(w_bits, "cuda")
+    oracle = om.grouped_gemm(a_bits, w_bits, off, act)
     offs = torch.from_numpy(off).cuda()
     s = torch.cuda.current_stream()
     nb = B.moe_grouped_gemm_workspace_bytes(G, R, N, K, act)
     ws = torch.zeros(max(nb, 256), dtype=torch.uint8, device="cuda")
     ref = torch.empty((R, N), dtype=torch.bfloat16, device="cuda")
     B.moe_grouped_gemm(a, w, offs, G, R, N, K, act, ref, ws, nb, s)
+    n_ref = B.moe_last_launch_count()
     ref64 = to_f64(ref)
     outs = []
     for _ in range(2):   # two calls in a row on the same fixed scratch
         out = torch.full((R, N), 3.0, dtype=torch.bfloat16, device="cuda")
         B.moe_grouped_gemm_noalloc(a, w, offs, G, R, N, K, act, out, s)
+        assert B.moe_last_launch_count() == n_ref >= 1
         assert B.moe_last_device_error(s) == 0
         got = to_f64(out)
         assert_close_layer(got, ref64, f"noalloc rows={rows} N={N} K={K} act={act}")
+        assert_close_layer(got, oracle, f"noalloc vs oracle rows={rows} N={N} K={K} act={act}")
         outs.append(out)
     torch.cuda.synchronize()
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
