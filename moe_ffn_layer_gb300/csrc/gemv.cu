@@ -315,7 +315,7 @@ bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows) {
 
 int grouped_gemv_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, cudaStream_t stream, int* launches,
-                        const int32_t* a_rows, int a_src_rows, int max_group_rows) {
+                        const int32_t* a_rows, int a_src_rows, int max_group_rows, int grid_cap) {
   if (rows_max == 0) return MOE_OK;
   // at most min(G, rows_max) non-empty groups
   const long long groups = G < rows_max ? G : rows_max;
@@ -331,7 +331,9 @@ int grouped_gemv_launch(const void* a, const void* w, const int32_t* offsets, in
   if (current_device_info(&dev_status, &sms) != MOE_OK) return MOE_ERR_CUDA;
   if (per_sm == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kGemvThreads, 0) != cudaSuccess)
     return MOE_ERR_CUDA;
-  const long long resident = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
+  // resident CTAs of the SMs the launch may fill
+  const long long resident = static_cast<long long>(grid_cap > 0 && grid_cap < sms ? grid_cap : sms) *
+                             (per_sm > 0 ? per_sm : 1);
   if (grid > resident) grid = resident;
   const dim3 g(static_cast<unsigned>(grid)), b(kGemvThreads);
   const cudaError_t rc = launch_chained(kernel, g, b, 0, stream, static_cast<const __nv_bfloat16*>(a),

@@ -922,7 +922,7 @@ int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, in
   const int bound = rows_max == 1 ? 1 : max_group_rows;
   if (act != 2 && grouped_gemv_applies(G, N, K, act, bound))
     return grouped_gemv_launch(a, w, offsets, G, rows_max, N, K, act, out, status, stream, launches, a_rows,
-                               a_src_rows, bound);
+                               a_src_rows, bound, grid_cap);
   if (grouped_gemm_weights_on_m(G, rows_max, N)) {
     if (act == 1)
       return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,

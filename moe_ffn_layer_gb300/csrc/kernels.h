@@ -61,9 +61,10 @@ int grouped_gemm_max_groups();
 // token adds at most one row per group) run on the CUDA cores: a weight stream
 // where a tensor-core tile would mostly hold padding.
 bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows);
+// grid_cap: SMs the launch may fill (0: all).
 int grouped_gemv_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, cudaStream_t stream, int* launches, const int32_t* a_rows,
-                        int a_src_rows, int max_group_rows);
+                        int a_src_rows, int max_group_rows, int grid_cap = 0);
 // One token: gmm2 over its k one-row groups and the combine in one launch
 // (out[H] = bf16(sum_j topk_w[j] * y_j + shared)), the same bits as the one-row
 // gmm2 followed by combine_launch.  h: [k][K] rows in group order; shared

@@ -415,6 +415,29 @@ def test_forward_sampled_full_size(name, T):
     assert_close_layer(to_f64(got), ref["out"], f"{name} T={T} sampled")
 
 
+@pytest.mark.parametrize("T", [4, 16])
+def test_forward_decode_sizes_of_the_wide_layer(T):
+    """Decode batches of the H=4096, E=256, I=1024 layer (the large-prefill
+    layer): the one-launch router with its dispatch, gmm1 reading the rows of x
+    by TMA gather4, gmm2."""
+    w = synth.workload("large_prefill", T)
+    ref = om.forward(inputs("large_prefill", T), w.k)
+    out = layer("large_prefill", T).forward(x_tensor("large_prefill", T))
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], f"large-prefill layer T={T}")
+
+
+@pytest.mark.parametrize("T", [2, 12, 16])
+def test_forward_decode_sizes(T):
+    """Decode batch sizes between and beyond the benchmark's (up to the
+    largest batch the one-launch router handles)."""
+    w = synth.workload("decode", T)
+    ref = om.forward(inputs("decode", T), w.k)
+    out = layer("decode", T).forward(x_tensor("decode", T))
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], f"decode T={T}")
+
+
 def test_forward_one_hot_expert_and_empty_experts():
     """Every token routed to one expert (a group of T rows spanning several
     128-row tiles with a ragged tail) while most experts stay empty; T above
@@ -445,6 +468,19 @@ def test_forward_decode_gathered_rows(T, I):
     out = L.forward(bf16_tensor(inp["x"], "cuda"))
     no_device_error()
     assert_close_layer(to_f64(out), ref["out"], f"gathered rows T={T} I={I}")
+
+
+def test_forward_one_token_wide_expert():
+    """One token with wide experts (I = 8192, K of gmm2 eight times the
+    decode layer's): gmm1 on the CUDA cores, then gmm2 and the combine in one
+    launch."""
+    wl = synth.Workload("wide", 1, 256, 8, 8, 8192, 64, sigma_router=0.1, sigma_w=0.02)
+    inp = synth.make_inputs(wl, 17)
+    ref = om.forward(inp, wl.k)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    out = L.forward(bf16_tensor(inp["x"], "cuda"))
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"], "one token, I = 8192")
 
 
 def test_forward_without_shared_expert():
@@ -566,7 +602,8 @@ def test_forward_one_token_matches_standalone_calls(case):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
-DISPATCH_CASES = [("decode", 1), ("decode", 4), ("decode", 8), ("tiny", 16), ("batched_decode", 64)]
+DISPATCH_CASES = [("decode", 1), ("decode", 4), ("decode", 8), ("decode", 16), ("tiny", 16),
+                  ("batched_decode", 64)]
 
 
 @pytest.mark.parametrize("name,T", DISPATCH_CASES)
@@ -661,4 +698,5 @@ def test_forward_repeatable_and_launch_count():
     b = L.forward(x)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    assert n >= 6
+    # shared gate_up and down; router with dispatch, gate_up, down, combine
+    assert n == 6

@@ -1,8 +1,9 @@
-"""The bounded-wait path of the grouped matmul, on the GPU without a fault:
-with the wait limit at 0 every mbarrier wait that is not already complete
-expires at once, the kernel records MOE_ERR_TIMEOUT, drains the copies it
-issued, frees its tensor memory and exits without writing its output.  With
-the limit restored, the next call gives the same bits as before."""
+"""The bounded-wait path, on the GPU without a fault.  With the wait limit at 0
+every wait that is not already complete expires at once: the grouped matmul
+records MOE_ERR_TIMEOUT, drains the copies it issued, frees its tensor memory
+and exits without writing its output.  With the limit restored, the next call
+gives the same bits as before (for the layer, once its workspace is zeroed
+again, as after any device error)."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +12,7 @@ from cases import assert_close_layer, to_f64
 from moe_ffn_layer_gb300 import binding as B
 from moe_ffn_layer_gb300 import build as build_mod
 from moe_ffn_layer_gb300 import synth
-from moe_ffn_layer_gb300.layer import bf16_tensor
+from moe_ffn_layer_gb300.layer import MoEFFN, bf16_tensor
 from oracle import moe_oracle as om
 
 pytestmark = pytest.mark.gpu
@@ -57,5 +58,28 @@ def test_wait_limit_expires_and_next_call_is_clean(rows, N, K, act):
 
     again = torch.empty_like(fresh)
     B.moe_grouped_gemm(a, w, offs, G, R, N, K, act, again, None, 0, s)
+    assert B.moe_last_device_error(s) == 0
+    assert torch.equal(again.view(torch.int16), fresh.view(torch.int16))
+
+
+def test_layer_forward_after_a_timeout_is_clean():
+    wl = synth.Workload("dec", 4, 512, 16, 4, 256, 128, sigma_router=0.1, sigma_w=0.03)
+    inp = synth.make_inputs(wl, 19)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    x = bf16_tensor(inp["x"], "cuda")
+    s = torch.cuda.current_stream()
+    fresh = L.forward(x).clone()
+    assert B.moe_last_device_error(s) == 0
+    assert_close_layer(to_f64(fresh), om.forward(inp, wl.k)["out"], "before")
+    try:
+        B.moe_debug_set_wait_limit_ns(0)
+        L.forward(x)
+    finally:
+        B.moe_debug_set_wait_limit_ns(DEFAULT_NS)
+    assert B.moe_last_device_error(s) == TIMEOUT
+    # after a device error the workspace is zeroed again (split-K tickets of the
+    # abandoned shared-expert matmuls may be left taken)
+    L.workspace(wl.T).zero_()
+    again = L.forward(x)
     assert B.moe_last_device_error(s) == 0
     assert torch.equal(again.view(torch.int16), fresh.view(torch.int16))
