@@ -2,7 +2,8 @@
 
 This module only draws numbers: hidden states, router weights, router bias and
 expert weights, rounded to the storage types the layer reads (bf16 stored as
-uint16 bit patterns, fp32 router).  It computes nothing of the layer itself.
+uint16 bit patterns, fp32 router; for the FP8 layer, e4m3 codes with one fp32
+scale per weight row, the storage format of the weights).  It computes nothing of the layer itself.
 The one place where it looks at the router is the near-tie guard: a token whose
 k-th and (k+1)-th router logits lie closer than ``GAP`` gets its hidden row
 redrawn, so that the choice of experts does not hinge on the summation order
@@ -84,6 +85,35 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     return ((u + r) >> 16).astype(np.uint16)
 
 
+# the 127 non-negative finite e4m3 values, ascending (code = index): exponent
+# field e (bias 7) and mantissa m; e = 0 holds m * 2^-9
+_E4M3_POS = np.array([(m * 2.0 ** -9) if (c >> 3) == 0 else (1 + m / 8.0) * 2.0 ** ((c >> 3) - 7)
+                      for c in range(127) for m in [c & 7]], dtype=np.float64)
+
+
+def f32_to_e4m3(v: np.ndarray) -> np.ndarray:
+    """Round float32 values to e4m3 codes (uint8), to nearest, ties to the even
+    code, magnitudes above 448 saturating to 448."""
+    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 126)   # first value >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a == _E4M3_POS[hi], hi, code)
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_rows_e4m3(w: np.ndarray):
+    """Per-row (output channel) e4m3 quantisation of float32 weights [..., K]:
+    scale = max|row| / 448 (fp32; 1 for an all-zero row), codes = e4m3(w /
+    scale).  Returns (codes uint8 [..., K], scale float32 [...])."""
+    w = np.asarray(w, dtype=np.float32)
+    amax = np.abs(w).max(axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    return f32_to_e4m3(w / scale[..., None]), scale
+
+
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
@@ -162,6 +192,38 @@ def make_expert_weights(w: Workload, seed: int = 0):
     with _cf.ThreadPoolExecutor(_threads()) as ex:
         list(ex.map(fill, range(w.E)))
     return wgu, wd
+
+
+def make_expert_weights_w8(w: Workload, seed: int = 0):
+    """Routed expert weights in e4m3 with one fp32 scale per output row: the
+    same fp32 draws as make_expert_weights, quantised row by row.  Returns
+    (gate_up codes [E][2I][H], gate_up scales [E][2I], down codes [E][H][I],
+    down scales [E][H])."""
+    wgu = np.empty((w.E, 2 * w.I, w.H), dtype=np.uint8)
+    sgu = np.empty((w.E, 2 * w.I), dtype=np.float32)
+    wd = np.empty((w.E, w.H, w.I), dtype=np.uint8)
+    sd = np.empty((w.E, w.H), dtype=np.float32)
+
+    def fill(e):
+        g = _rng(seed, 4, e).standard_normal((2 * w.I, w.H), dtype=np.float32) * np.float32(w.sigma_w)
+        wgu[e], sgu[e] = quantize_rows_e4m3(g)
+        d = _rng(seed, 5, e).standard_normal((w.H, w.I), dtype=np.float32) * np.float32(w.sigma_w)
+        wd[e], sd[e] = quantize_rows_e4m3(d)
+
+    with _cf.ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(fill, range(w.E)))
+    return wgu, sgu, wd, sd
+
+
+def make_inputs_w8(w: Workload, seed: int = 0) -> dict:
+    """All inputs of one layer forward with e4m3 routed expert weights (keys
+    w_gate_up / w_down hold codes, w_gate_up_scale / w_down_scale the row
+    scales); x, the router and the bf16 shared expert as make_inputs."""
+    x, wr, b = make_activations(w, seed)
+    wgu, sgu, wd, sd = make_expert_weights_w8(w, seed)
+    shg, shd = make_shared_weights(w, seed)
+    return dict(x=x, w_router=wr, bias=b, w_gate_up=wgu, w_gate_up_scale=sgu, w_down=wd, w_down_scale=sd,
+                ws_gate_up=shg, ws_down=shd)
 
 
 def make_shared_weights(w: Workload, seed: int = 0):

@@ -29,11 +29,22 @@ permuted layout are grouped by expert (ascending) and, within an expert, by
 token (ascending).  The router's top-k decision is taken on fp32 logits, the
 precision the layer fixes for the router; everything after it is float64.
 
+FP8 expert weights (the w8a8_dynamic matmul configuration of the xLLM PR
+"FlashComm1 + matmul-reduce-scatter", configuration section, read for the
+weight side only): each routed expert's weight rows are stored as e4m3 codes
+(OCP 8-bit float: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits,
+exponent 0 holding the subnormals m * 2^-9, codes 0x7f/0xff NaN, no infinity)
+with one fp32 scale per row (output channel): W[n][k] = e4m3(q[n][k]) * s[n].
+The layer is the same layer with those weights; activations stay bf16 and the
+shared expert stays bf16 (the MoE page keeps it unquantised).
+
 Parity pins (tests/test_oracle.py): brute-force fp64 top-k, the full-softmax
 closed form, numpy's stable argsort for the permutation, a dense SwiGLU MLP in
 torch for E=1, a brute-force dense evaluation of every expert on every token
 masked by the routing weights, the identical-experts invariant, linearity in the
-down weights, and a hand-derived closed-form example (tests/golden/).
+down weights, a hand-derived closed-form example (tests/golden/), torch's
+float8_e4m3fn decoding of every code, and the FP8 layer equal to the bf16
+layer when the bf16 weights are exactly e4m3 codes times their row scales.
 """
 from __future__ import annotations
 
@@ -53,6 +64,44 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return u.view(np.float32)
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact value of e4m3 codes (uint8): sign bit 7, exponent bits 6..3 (bias
+    7), mantissa bits 2..0; exponent 0 gives m * 2^-9, otherwise
+    (1 + m/8) * 2^(e-7); 0x7f and 0xff are NaN."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
+def dequant_w8(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """Weights of e4m3 codes [..., rows, K] with one fp32 scale per row
+    [..., rows]: value times scale, float64 (exact)."""
+    return e4m3_to_f64(codes) * np.asarray(scale, dtype=np.float32).astype(np.float64)[..., None]
+
+
+def is_w8(inp: dict) -> bool:
+    """The routed expert weights are e4m3 codes with row scales."""
+    return "w_gate_up_scale" in inp
+
+
+def expert_gate_up(inp: dict, e: int) -> np.ndarray:
+    """float64 gate_up weights [2I][H] of routed expert e."""
+    if is_w8(inp):
+        return dequant_w8(inp["w_gate_up"][e], inp["w_gate_up_scale"][e])
+    return bf16_to_f64(inp["w_gate_up"][e])
+
+
+def expert_down(inp: dict, e: int) -> np.ndarray:
+    """float64 down weights [H][I] of routed expert e."""
+    if is_w8(inp):
+        return dequant_w8(inp["w_down"][e], inp["w_down_scale"][e])
+    return bf16_to_f64(inp["w_down"][e])
 
 
 # ----------------------------------------------------------------------------
@@ -131,26 +180,27 @@ def silu(v: np.ndarray) -> np.ndarray:
         return v / (1.0 + np.exp(-v))
 
 
-def gate_up(a: np.ndarray, w_gate_up_bits: np.ndarray) -> np.ndarray:
-    """gmm1 + activation for one expert: W is [2N][K], rows 0..N-1 gate,
-    N..2N-1 up; returns SiLU(a.Wg^T) * (a.Wu^T), float64 [rows, N]."""
-    w = bf16_to_f64(w_gate_up_bits)
+def gate_up(a: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """gmm1 + activation for one expert: W (float64) is [2N][K], rows 0..N-1
+    gate, N..2N-1 up; returns SiLU(a.Wg^T) * (a.Wu^T), float64 [rows, N]."""
     n = w.shape[0] // 2
     g = a @ w[:n].T
     u = a @ w[n:].T
     return silu(g) * u
 
 
-def down(h: np.ndarray, w_down_bits: np.ndarray) -> np.ndarray:
-    """gmm2 for one expert: h.Wd^T with Wd [N_out][K]."""
-    return h @ bf16_to_f64(w_down_bits).T
+def down(h: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """gmm2 for one expert: h.Wd^T with Wd (float64) [N_out][K]."""
+    return h @ w.T
 
 
-def grouped_gemm(a_bits: np.ndarray, w_bits: np.ndarray, offsets: np.ndarray, act: int):
+def grouped_gemm(a_bits: np.ndarray, w_bits: np.ndarray, offsets: np.ndarray, act: int, w_scale=None):
     """Rows [off_g, off_{g+1}) of A times group g's weights (W[g] K-major).
 
     act 0: out = A_g . W_g^T (W [G][N][K]); act 1: out = SiLU(A_g.Wg^T)*(A_g.Wu^T)
-    (W [G][2N][K]).  float64 [rows, N]; rows past offsets[G] are left at 0.
+    (W [G][2N][K]).  W is bf16 bits, or e4m3 codes when w_scale ([G][rows]
+    fp32, one per weight row) is given.  float64 [rows, N]; rows past
+    offsets[G] are left at 0.
     """
     a = bf16_to_f64(a_bits)
     G = w_bits.shape[0]
@@ -159,8 +209,8 @@ def grouped_gemm(a_bits: np.ndarray, w_bits: np.ndarray, offsets: np.ndarray, ac
     for g in range(G):
         r0, r1 = int(offsets[g]), int(offsets[g + 1])
         if r1 > r0:
-            out[r0:r1] = gate_up(a[r0:r1], w_bits[g]) if act == 1 else \
-                (a[r0:r1] @ bf16_to_f64(w_bits[g]).T)
+            w = bf16_to_f64(w_bits[g]) if w_scale is None else dequant_w8(w_bits[g], w_scale[g])
+            out[r0:r1] = gate_up(a[r0:r1], w) if act == 1 else (a[r0:r1] @ w.T)
     return out
 
 
@@ -168,7 +218,7 @@ def shared_expert(x: np.ndarray, ws_gate_up_bits, ws_down_bits) -> np.ndarray:
     """Shared expert on the hidden states: down(gate_up(x)); zero when absent."""
     if ws_gate_up_bits is None:
         return np.zeros_like(x)
-    return down(gate_up(x, ws_gate_up_bits), ws_down_bits)
+    return down(gate_up(x, bf16_to_f64(ws_gate_up_bits)), bf16_to_f64(ws_down_bits))
 
 
 # ----------------------------------------------------------------------------
@@ -200,8 +250,8 @@ def forward(inp: dict, k: int) -> dict:
     for e in range(E):
         r0, r1 = int(offsets[e]), int(offsets[e + 1])
         if r1 > r0:
-            h[r0:r1] = gate_up(x_perm[r0:r1], inp["w_gate_up"][e])
-            y[r0:r1] = down(h[r0:r1], inp["w_down"][e])
+            h[r0:r1] = gate_up(x_perm[r0:r1], expert_gate_up(inp, e))
+            y[r0:r1] = down(h[r0:r1], expert_down(inp, e))
     s = shared_expert(x, inp["ws_gate_up"], inp["ws_down"])
     out = combine(y, inv_perm, wts, s)
     return dict(ids=ids, w=wts, logits=logits, offsets=offsets, sorted_token=sorted_token,
@@ -231,8 +281,8 @@ def forward_tokens(inp: dict, k: int, tokens, routing=None) -> dict:
             by_expert.setdefault(int(ids[t, j]), []).append((i, j))
     for e, pairs in by_expert.items():
         rows = np.array([i for i, _ in pairs])
-        he = gate_up(x[rows], inp["w_gate_up"][e])
-        ye = down(he, inp["w_down"][e])
+        he = gate_up(x[rows], expert_gate_up(inp, e))
+        ye = down(he, expert_down(inp, e))
         for q, (i, j) in enumerate(pairs):
             h[i, j] = he[q]
             y[i, j] = ye[q]

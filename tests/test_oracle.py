@@ -230,3 +230,67 @@ def test_grouped_gemm_definition():
     out1 = om.grouped_gemm(a, wt, off, 1)
     gate, up = A[:4] @ W[0, :4].T, A[:4] @ W[0, 4:].T
     np.testing.assert_allclose(out1[:4], gate * torch.sigmoid(torch.from_numpy(gate)).numpy() * up, rtol=1e-12)
+
+
+# ---------------------------------------------------------------- FP8 expert weights
+
+def test_e4m3_decoding_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = om.e4m3_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.nonzero(nan)[0], [0x7F, 0xFF])
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # the format's landmarks: smallest subnormal, smallest normal, largest finite
+    assert got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6 and got[0x7E] == 448.0 and got[0xFE] == -448.0
+
+
+def test_w8_layer_equals_bf16_layer_on_exactly_representable_weights():
+    """When every bf16 weight is an e4m3 value times a power-of-two row scale,
+    the FP8 layer (codes and scales) and the bf16 layer are the same layer."""
+    w = synth.Workload("w8", 9, 64, 6, 2, 32, 48, sigma_router=0.3)
+    inp = synth.make_inputs(w, 5)
+    rng = np.random.default_rng(6)
+    vals = om.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+    def rows(shape):
+        codes = rng.integers(0, 0x7F, size=shape).astype(np.uint8) | (rng.integers(0, 2, size=shape) << 7).astype(np.uint8)
+        scale = np.exp2(rng.integers(-12, -6, size=shape[:-1])).astype(np.float32)
+        dense = (om.e4m3_to_f64(codes) * scale[..., None]).astype(np.float32)
+        bits = synth.f32_to_bf16_bits(dense)
+        assert np.array_equal(om.bf16_to_f64(bits), om.e4m3_to_f64(codes) * scale[..., None])   # exact in bf16
+        return codes, scale, bits
+    cgu, sgu, bgu = rows((w.E, 2 * w.I, w.H))
+    cd, sd, bd = rows((w.E, w.H, w.I))
+    inp_bf16 = dict(inp, w_gate_up=bgu, w_down=bd)
+    inp_w8 = dict(inp, w_gate_up=cgu, w_gate_up_scale=sgu, w_down=cd, w_down_scale=sd)
+    a, b = om.forward(inp_bf16, w.k), om.forward(inp_w8, w.k)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["h"], b["h"])
+    t = np.array([0, 4, 8])
+    assert np.array_equal(om.forward_tokens(inp_w8, w.k, t)["out"], om.forward_tokens(inp_bf16, w.k, t)["out"])
+    off = a["offsets"]
+    xp = inp["x"][a["sorted_token"]]
+    assert np.array_equal(om.grouped_gemm(xp, cgu, off, 1, w_scale=sgu), om.grouped_gemm(xp, bgu, off, 1))
+
+
+def test_w8_brute_force_dense_layer():
+    """FP8 layer against a dense evaluation of every expert on every token
+    (torch, float64 dequantised weights) masked by the routing weights."""
+    w = synth.Workload("w8d", 10, 64, 6, 2, 32, 48, sigma_router=0.3)
+    inp = synth.make_inputs_w8(w, 7)
+    r = om.forward(inp, w.k)
+    x = torch.from_numpy(om.bf16_to_f64(inp["x"]))
+    dense = torch.zeros((w.T, w.H), dtype=torch.float64)
+    for e in range(w.E):
+        wgu = torch.from_numpy(om.dequant_w8(inp["w_gate_up"][e], inp["w_gate_up_scale"][e]))
+        wd = torch.from_numpy(om.dequant_w8(inp["w_down"][e], inp["w_down_scale"][e]))
+        y = (torch.nn.functional.silu(x @ wgu[:w.I].T) * (x @ wgu[w.I:].T)) @ wd.T
+        mask = torch.zeros(w.T, dtype=torch.float64)
+        for t in range(w.T):
+            for j in range(w.k):
+                if r["ids"][t, j] == e:
+                    mask[t] = r["w"][t, j]
+        dense += mask[:, None] * y
+    sgu, sd = (torch.from_numpy(om.bf16_to_f64(a)) for a in (inp["ws_gate_up"], inp["ws_down"]))
+    dense += (torch.nn.functional.silu(x @ sgu[:w.Is].T) * (x @ sgu[w.Is:].T)) @ sd.T
+    np.testing.assert_allclose(r["out"], dense.numpy(), rtol=1e-10, atol=1e-12)
