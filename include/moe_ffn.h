@@ -177,6 +177,26 @@ MOE_API int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_
 MOE_API int moe_grouped_gemm_noalloc(const void* a, const void* w, const int32_t* group_offsets, int G, int rows_max,
                                      int N, int K, int act, void* out, cudaStream_t stream);
 
+/* GroupedMatmul with FP8 weights (the w8a8_dynamic matmul configuration of the
+ * xLLM PR "FlashComm1 + matmul-reduce-scatter", configuration section, taken
+ * for the weight side; activations stay bf16): W holds e4m3 codes (OCP 8-bit
+ * float: sign, 4 exponent bits with bias 7, 3 mantissa bits; the NaN codes
+ * 0x7f/0xff are not valid weights) with one fp32 scale per weight row, and the
+ * product uses W[g][n][k] = e4m3(code) * w_scale[g][n]:
+ *   act == 0:  out[r, n] = s[g][n] * (A[r] . code[g][n])          w  [G][N][K]
+ *   act == 1:  out[r, n] = SiLU(s_g * A[r].Wg[n]) * (s_u * A[r].Wu[n])
+ *              w [G][2N][K], rows 0..N-1 gate; w_scale [G][2N]
+ *  w_scale  fp32 [G][rows of W[g]] (device)
+ * Other arguments, scratch, checks and the result type as moe_grouped_gemm.
+ * Weight-streaming shapes only (the regime whose bytes the format halves):
+ * rows_max <= 64 * G, or rows_max == 1; others give MOE_ERR_UNSUPPORTED.  The
+ * codes are widened to bf16 in shared memory (exact), multiplied on the
+ * tensor cores with fp32 accumulation, and each row's scale is applied to the
+ * finished sum. */
+MOE_API int moe_grouped_gemm_w8(const void* a, const void* w, const float* w_scale, const int32_t* group_offsets,
+                                int G, int rows_max, int N, int K, int act, void* out, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
 /* Combine: out[t] = bf16( sum_j topk_w[t,j] * y[inv_perm[t*k+j]] + shared[t] ),
  * accumulated in fp32 in slot order j = 0..k-1, then the shared row.
  *  y bf16 [T*k][H];  inv_perm int32 [T*k];  topk_w fp32 [T][k]
@@ -203,6 +223,30 @@ MOE_API size_t moe_workspace_bytes(const moe_dims* d, int T);
 MOE_API int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, void* out, void* ws,
                 size_t ws_bytes, cudaStream_t stream, cudaStream_t side, cudaEvent_t ev_fork,
                 cudaEvent_t ev_join);
+
+/* The layer with FP8 routed expert weights (see moe_grouped_gemm_w8):
+ *  w_gate_up e4m3 [E][2I][H] with s_gate_up fp32 [E][2I];
+ *  w_down    e4m3 [E][H][I]  with s_down    fp32 [E][H];
+ * router and shared expert as in moe_weights (the shared expert stays bf16, as
+ * the page on MoE multi-stream overlap runs it: bf16, unquantised). */
+typedef struct {
+  const float* w_router;
+  const float* router_bias;
+  const void* w_gate_up;
+  const float* s_gate_up;
+  const void* w_down;
+  const float* s_down;
+  const void* ws_gate_up;
+  const void* ws_down;
+} moe_weights_w8;
+
+/* moe_forward with FP8 routed expert weights.  Same streams, events,
+ * workspace (moe_workspace_bytes) and results as moe_forward, the routed
+ * matmuls reading 1-byte weights.  Decode-sized batches: T*k <= 64*E (the
+ * weights-on-M form); larger batches give MOE_ERR_UNSUPPORTED. */
+MOE_API int moe_forward_w8(const moe_dims* d, const moe_weights_w8* w, const void* x, int T, void* out, void* ws,
+                           size_t ws_bytes, cudaStream_t stream, cudaStream_t side, cudaEvent_t ev_fork,
+                           cudaEvent_t ev_join);
 
 /* Reads and clears the current device's status word (first device-side error
  * since the last read, MOE_OK if none).  Synchronises `stream`. */

@@ -29,6 +29,12 @@ class moe_dims(ctypes.Structure):
                 ("I_s", ctypes.c_int)]
 
 
+class moe_weights_w8(ctypes.Structure):
+    _fields_ = [("w_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p),
+                ("s_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
+                ("ws_gate_up", ctypes.c_void_p), ("ws_down", ctypes.c_void_p)]
+
+
 class moe_workspace_offsets(ctypes.Structure):
     _fields_ = [("topk_ids", ctypes.c_size_t), ("topk_w", ctypes.c_size_t), ("expert_offsets", ctypes.c_size_t),
                 ("sorted_token", ctypes.c_size_t), ("inv_perm", ctypes.c_size_t)]
@@ -48,10 +54,13 @@ _SIGS = {
     "moe_grouped_gemm_workspace_bytes": (_Z, [_I, _I, _I, _I, _I]),
     "moe_grouped_gemm": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_grouped_gemm_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "moe_grouped_gemm_w8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_unpermute_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_workspace_bytes": (_Z, [ctypes.POINTER(moe_dims), _I]),
     "moe_forward": (_I, [ctypes.POINTER(moe_dims), ctypes.POINTER(moe_weights), _P, _I, _P, _P, _Z, _P, _P, _P,
                          _P]),
+    "moe_forward_w8": (_I, [ctypes.POINTER(moe_dims), ctypes.POINTER(moe_weights_w8), _P, _I, _P, _P, _Z, _P, _P,
+                            _P, _P]),
     "moe_last_device_error": (_I, [_P]),
     "moe_last_launch_count": (_I, []),
     "moe_workspace_layout": (_I, [ctypes.POINTER(moe_dims), _I, ctypes.POINTER(moe_workspace_offsets)]),
@@ -144,6 +153,12 @@ def moe_grouped_gemm_noalloc(a, w, group_offsets, G, rows_max, N, K, act, out, s
                                                                              handle(stream)))
 
 
+def moe_grouped_gemm_w8(a, w, w_scale, group_offsets, G, rows_max, N, K, act, out, ws, ws_bytes, stream) -> int:
+    return _check("moe_grouped_gemm_w8", lib().moe_grouped_gemm_w8(ptr(a), ptr(w), ptr(w_scale), ptr(group_offsets),
+                                                                   G, rows_max, N, K, act, ptr(out), ptr(ws),
+                                                                   ws_bytes, handle(stream)))
+
+
 def moe_unpermute_combine(y, inv_perm, topk_w, shared, T, H, k, out, stream) -> int:
     return _check("moe_unpermute_combine", lib().moe_unpermute_combine(ptr(y), ptr(inv_perm), ptr(topk_w),
                                                                        ptr(shared), T, H, k, ptr(out),
@@ -159,6 +174,13 @@ def moe_forward(dims: moe_dims, weights: moe_weights, x, T, out, ws, ws_bytes, s
     return _check("moe_forward", lib().moe_forward(ctypes.byref(dims), ctypes.byref(weights), ptr(x), T, ptr(out),
                                                    ptr(ws), ws_bytes, handle(stream), handle(side),
                                                    handle(ev_fork), handle(ev_join)))
+
+
+def moe_forward_w8(dims: moe_dims, weights: moe_weights_w8, x, T, out, ws, ws_bytes, stream, side, ev_fork,
+                   ev_join) -> int:
+    return _check("moe_forward_w8", lib().moe_forward_w8(ctypes.byref(dims), ctypes.byref(weights), ptr(x), T,
+                                                         ptr(out), ptr(ws), ws_bytes, handle(stream), handle(side),
+                                                         handle(ev_fork), handle(ev_join)))
 
 
 def moe_last_device_error(stream) -> int:

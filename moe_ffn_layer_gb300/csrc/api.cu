@@ -273,6 +273,33 @@ int moe_grouped_gemm(const void* a, const void* w, const int32_t* group_offsets,
   return rc;
 }
 
+int moe_grouped_gemm_w8(const void* a, const void* w, const float* w_scale, const int32_t* group_offsets, int G,
+                        int rows_max, int N, int K, int act, void* out, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+  t_last_launches = 0;
+  if (G <= 0 || rows_max < 0 || N <= 0 || K <= 0 || (act != 0 && act != 1)) return MOE_ERR_INVALID;
+  if (!group_offsets && G != 1) return MOE_ERR_INVALID;
+  if (G > moe::grouped_gemm_max_groups() || N % 64 || K % 64) return MOE_ERR_UNSUPPORTED;
+  // 8-bit weights: groups of few rows (the weights-on-M form), decode-sized batches
+  if (!moe::grouped_gemm_weights_on_m(G, rows_max, N) && rows_max != 1) return MOE_ERR_UNSUPPORTED;
+  if (rows_max == 0) return MOE_OK;
+  if (!a || !w || !w_scale || !out) return MOE_ERR_INVALID;
+  if (!al16(a) || !al16(w) || !al16(out) || (reinterpret_cast<uintptr_t>(group_offsets) & 3u) ||
+      (reinterpret_cast<uintptr_t>(w_scale) & 3u) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_UNSUPPORTED;
+  if (!moe::device_local(a) || !moe::device_local(w) || !moe::device_local(out)) return MOE_ERR_UNSUPPORTED;
+  DevInfo* di = nullptr;
+  int rc = dev_info(&di);
+  if (rc) return rc;
+  if (ws && ws_bytes < moe::grouped_gemm_ws_bytes(G, rows_max, N, act)) return MOE_ERR_WORKSPACE;
+  int n = 0;
+  const moe::GemmScratch scratch = moe::grouped_gemm_scratch(ws, ws_bytes);
+  rc = moe::grouped_gemm_launch(a, w, group_offsets, G, rows_max, N, K, act, out, di->status, &scratch, di->sms,
+                                stream, &n, nullptr, 0, 0, 0, w_scale);
+  t_last_launches = n;
+  return rc;
+}
+
 int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const float* topk_w, const void* shared, int T,
                           int H, int k, void* out, cudaStream_t stream) {
   t_last_launches = 0;
@@ -293,13 +320,38 @@ size_t moe_workspace_bytes(const moe_dims* d, int T) {
   return layout(d, T).total;
 }
 
-int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, void* out, void* ws,
-                size_t ws_bytes, cudaStream_t stream, cudaStream_t side, cudaEvent_t ev_fork, cudaEvent_t ev_join) {
+}  // extern "C"
+
+namespace {
+
+// The weights of a layer forward: routed experts in bf16 (scales null) or
+// e4m3 with one fp32 scale per weight row; router and shared expert as in
+// moe_weights.
+struct LayerWeights {
+  const float* w_router;
+  const float* router_bias;
+  const void* w_gate_up;
+  const float* s_gate_up;
+  const void* w_down;
+  const float* s_down;
+  const void* ws_gate_up;
+  const void* ws_down;
+};
+
+int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T, void* out, void* ws, size_t ws_bytes,
+                 cudaStream_t stream, cudaStream_t side, cudaEvent_t ev_fork, cudaEvent_t ev_join) {
   t_last_launches = 0;
   int rc = check_dims(d);
   if (rc) return rc;
   if (!w || T < 0) return MOE_ERR_INVALID;
   if (static_cast<long long>(T) * d->k > 0x7fffffffLL) return MOE_ERR_UNSUPPORTED;
+  const bool w8 = w->s_gate_up != nullptr;
+  if (w8 && !w->s_down) return MOE_ERR_INVALID;
+  // 8-bit routed weights: the weights-on-M matmuls (and one-row groups) only
+  if (w8 && !moe::grouped_gemm_weights_on_m(d->E, T * d->k, d->I)) return MOE_ERR_UNSUPPORTED;
+  if (w8 && !moe::grouped_gemm_weights_on_m(d->E, T * d->k, d->H)) return MOE_ERR_UNSUPPORTED;
+  if (w8 && ((reinterpret_cast<uintptr_t>(w->s_gate_up) & 3u) || (reinterpret_cast<uintptr_t>(w->s_down) & 3u)))
+    return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   const bool has_shared = d->I_s > 0;
   if (!x || !out || !ws || !w->w_router || !w->w_gate_up || !w->w_down) return MOE_ERR_INVALID;
@@ -394,23 +446,49 @@ int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, v
     // cannot feed full 128-row tiles
     rc = T <= moe::route_small_max_tokens()
              ? moe::grouped_gemm_launch(x, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, &gmain,
-                                        main_sms, stream, &n, sorted, T, 0, T)
+                                        main_sms, stream, &n, sorted, T, 0, T, w->s_gate_up)
              : moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status,
-                                        &gmain, di->sms, stream, &n);
+                                        &gmain, di->sms, stream, &n, nullptr, 0, 0, 0, w->s_gate_up);
   // one token: gmm2 and the combine in one launch, after the join (the shared
   // expert has long finished by then: it streamed its weights during routing)
   const bool fused_tail = T == 1 && moe::down_combine_gemv_applies(d->E, d->H, d->I, d->k);
   if (!rc && !fused_tail)
     rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, &gmain,
-                                  main_sms, stream, &n, nullptr, 0, 0, T);
+                                  main_sms, stream, &n, nullptr, 0, 0, T, w->s_down);
   if (rc) return rc;
   // join, then combine
   if (has_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
-  rc = fused_tail ? moe::down_combine_gemv_launch(h, w->w_down, offsets, d->E, d->H, d->I, d->k, inv, tw,
+  rc = fused_tail ? moe::down_combine_gemv_launch(h, w->w_down, w->s_down, offsets, d->E, d->H, d->I, d->k, inv, tw,
                                                   has_shared ? s : nullptr, out, di->status, stream, &n)
                   : moe::combine_launch(y, inv, tw, has_shared ? s : nullptr, T, d->H, d->k, rows, out, stream, &n);
   t_last_launches = n;
   return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_forward(const moe_dims* d, const moe_weights* w, const void* x, int T, void* out, void* ws,
+                size_t ws_bytes, cudaStream_t stream, cudaStream_t side, cudaEvent_t ev_fork, cudaEvent_t ev_join) {
+  if (!w) {
+    t_last_launches = 0;
+    return MOE_ERR_INVALID;
+  }
+  const LayerWeights lw{w->w_router, w->router_bias, w->w_gate_up, nullptr, w->w_down, nullptr, w->ws_gate_up,
+                        w->ws_down};
+  return forward_impl(d, &lw, x, T, out, ws, ws_bytes, stream, side, ev_fork, ev_join);
+}
+
+int moe_forward_w8(const moe_dims* d, const moe_weights_w8* w, const void* x, int T, void* out, void* ws,
+                   size_t ws_bytes, cudaStream_t stream, cudaStream_t side, cudaEvent_t ev_fork, cudaEvent_t ev_join) {
+  if (!w || !w->s_gate_up || !w->s_down) {
+    t_last_launches = 0;
+    return MOE_ERR_INVALID;
+  }
+  const LayerWeights lw{w->w_router, w->router_bias, w->w_gate_up, w->s_gate_up, w->w_down, w->s_down,
+                        w->ws_gate_up, w->ws_down};
+  return forward_impl(d, &lw, x, T, out, ws, ws_bytes, stream, side, ev_fork, ev_join);
 }
 
 int moe_last_device_error(cudaStream_t stream) {

@@ -196,6 +196,10 @@ __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map
       : "memory");
 }
 
+// Orders this thread's earlier shared-memory writes (generic proxy) before
+// later async-proxy reads of them (tcgen05.mma operands, TMA stores).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Four rows r0..r3 of a 2-D tensor (box one row high, 64 bf16 wide) to four
 // consecutive 128-byte rows at dst (TMA tile::gather4).
 __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int r0, int r1,
@@ -342,5 +346,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------- e4m3
+// An e4m3 code (sign bit 7, exponent bits 6..3 with bias 7, mantissa bits
+// 2..0) as float.  Its exponent and mantissa bits placed in an f32's exponent
+// and mantissa fields give 2^(e-127) * 1.m, or the subnormal 0.m * 2^-126 for
+// e = 0; multiplying by 2^120 moves the bias from 127 to 7, so the result is
+// the code's exact value (the NaN codes 0x7f/0xff, which stored weights never
+// hold, read as +-480).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  return __uint_as_float(((c & 0x7Fu) << 20) | ((c & 0x80u) << 24)) * 0x1p120f;
+}
+
+// The two e4m3 codes in bits 0..15 of w (bits 0..7 first) as a bf16 pair (the
+// first in the low half).  Every e4m3 value has at most four significant bits,
+// so the upper half of its f32 bits is its exact bf16 encoding.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w) {
+  return __byte_perm(__float_as_uint(e4m3_to_f32(w)), __float_as_uint(e4m3_to_f32(w >> 8)), 0x7632);
+}
+
+// Eight e4m3 codes (v.x bytes 0..3, then v.y) as floats.
+__device__ __forceinline__ void e4m3x8_to_f32(const uint2& v, float (&f)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[i] = e4m3_to_f32(v.x >> (8 * i));
+    f[4 + i] = e4m3_to_f32(v.y >> (8 * i));
+  }
+}
 
 }  // namespace moe

@@ -20,6 +20,8 @@
 // CTAs walk the (non-empty group, output block) items) and each CTA lists the
 // non-empty groups once, with all offsets loaded in one round.  For one token
 // gmm2 and the combine also run as one launch (down_combine_gemv_kernel).
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -35,6 +37,25 @@ __device__ __forceinline__ void bf16x8(const uint4& v, float (&f)[8]) {
   f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
   f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
+
+// Eight consecutive weights of a row: bf16 (WT 0, 16 bytes) or e4m3 codes (WT
+// 1, 8 bytes; the row's scale is applied to the finished dot product).
+template <int WT>
+struct WeightChunk;
+template <>
+struct WeightChunk<0> {
+  using Vec = uint4;
+  __device__ static Vec load(const uint8_t* row, int k) { return __ldg(reinterpret_cast<const uint4*>(row + 2 * k)); }
+  __device__ static void to_f32(const Vec& v, float (&f)[8]) { bf16x8(v, f); }
+  static constexpr int kBytes = 2;
+};
+template <>
+struct WeightChunk<1> {
+  using Vec = uint2;
+  __device__ static Vec load(const uint8_t* row, int k) { return __ldg(reinterpret_cast<const uint2*>(row + k)); }
+  __device__ static void to_f32(const Vec& v, float (&f)[8]) { e4m3x8_to_f32(v, f); }
+  static constexpr int kBytes = 1;
+};
 
 // The non-empty groups in ascending order into s_groups, their number into
 // *s_count (every thread of the CTA takes part; one round of offset loads).  A
@@ -94,13 +115,15 @@ __device__ __forceinline__ void list_groups(const int32_t* __restrict__ offsets,
 // ACT 1: out[r][n] = silu(a[r].Wg[n]) * (a[r].Wu[n]), W[g] = [2N][K] (gate rows
 // first); ACT 0: out[r][n] = a[r].W[g][n], W[g] = [N][K].  Token row r of the
 // product is row a_rows[r] of `a` when a_rows is given, else row r.  R >= the
-// rows of any group (1, 2 or 4).
-template <int ACT, int R>
+// rows of any group (1, 2 or 4).  WT 1: W holds e4m3 codes and wscale one fp32
+// scale per weight row ([G][2N] or [G][N]), applied to each dot product.
+template <int ACT, int R, int WT>
 __global__ void __launch_bounds__(kGemvThreads)
-    grouped_gemv_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ w,
-                        const int32_t* __restrict__ offsets, int G, int rows_max, int N, int K,
-                        const int32_t* __restrict__ a_rows, int a_src_rows, __nv_bfloat16* __restrict__ out,
-                        int* status) {
+    grouped_gemv_kernel(const __nv_bfloat16* __restrict__ a, const uint8_t* __restrict__ w,
+                        const float* __restrict__ wscale, const int32_t* __restrict__ offsets, int G, int rows_max,
+                        int N, int K, const int32_t* __restrict__ a_rows, int a_src_rows,
+                        __nv_bfloat16* __restrict__ out, int* status) {
+  using WC = WeightChunk<WT>;
   constexpr int NW = ACT == 1 ? 2 : kRowsDown;   // weight rows per warp
   constexpr int NPW = ACT == 1 ? 1 : kRowsDown;  // output columns per warp
   __shared__ int s_groups[kMaxGemvGroups];
@@ -119,11 +142,12 @@ __global__ void __launch_bounds__(kGemvThreads)
   const int nr = (offsets ? offsets[g + 1] : rows_max) - r0;
   // this warp's weight rows and token rows (rows past nr repeat the last one)
   const size_t wrows = ACT == 1 ? 2 * static_cast<size_t>(N) : N;
-  const __nv_bfloat16* wr[NW];
+  const uint8_t* wr[NW];
+  size_t wrow_idx[NW];
 #pragma unroll
   for (int i = 0; i < NW; ++i) {
-    const size_t row = ACT == 1 ? (i == 0 ? n0 : N + n0) : n0 + i;
-    wr[i] = w + (static_cast<size_t>(g) * wrows + row) * K;
+    wrow_idx[i] = static_cast<size_t>(g) * wrows + (ACT == 1 ? (i == 0 ? n0 : N + n0) : n0 + i);
+    wr[i] = w + wrow_idx[i] * K * WC::kBytes;
   }
   const __nv_bfloat16* ar[R];
 #pragma unroll
@@ -141,13 +165,14 @@ __global__ void __launch_bounds__(kGemvThreads)
   // kSteps strides of K per pass: every load of a pass goes out before its
   // first FMA (a lane keeps kSteps * (NW + R) 16-byte loads in flight)
   for (int kb = lane * 8; kb < K; kb += 256 * kSteps) {
-    uint4 wv[kSteps][NW], av[kSteps][R];
+    typename WC::Vec wv[kSteps][NW];
+    uint4 av[kSteps][R];
 #pragma unroll
     for (int u = 0; u < kSteps; ++u) {
       const int k0 = kb + u * 256;
       if (k0 < K) {
 #pragma unroll
-        for (int i = 0; i < NW; ++i) wv[u][i] = __ldg(reinterpret_cast<const uint4*>(wr[i] + k0));
+        for (int i = 0; i < NW; ++i) wv[u][i] = WC::load(wr[i], k0);
 #pragma unroll
         for (int j = 0; j < R; ++j) av[u][j] = __ldg(reinterpret_cast<const uint4*>(ar[j] + k0));
       }
@@ -162,7 +187,7 @@ __global__ void __launch_bounds__(kGemvThreads)
 #pragma unroll
         for (int i = 0; i < NW; ++i) {
           float wf[8];
-          bf16x8(wv[u][i], wf);
+          WC::to_f32(wv[u][i], wf);
           float s = acc[i][j];
 #pragma unroll
           for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
@@ -178,16 +203,19 @@ __global__ void __launch_bounds__(kGemvThreads)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc[i][j] += __shfl_xor_sync(0xffffffffu, acc[i][j], o);
   if (lane == 0) {
+    float sc[NW];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) sc[i] = WT ? __ldg(wscale + wrow_idx[i]) : 1.f;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       if (j >= nr) break;
       __nv_bfloat16* orow = out + static_cast<size_t>(r0 + j) * N + n0;
       if (ACT == 1) {
-        const float gt = acc[0][j], up = acc[1][j];
+        const float gt = WT ? acc[0][j] * sc[0] : acc[0][j], up = WT ? acc[1][j] * sc[1] : acc[1][j];
         orow[0] = __float2bfloat16_rn(gt / (1.0f + __expf(-gt)) * up);
       } else {
 #pragma unroll
-        for (int i = 0; i < NPW; ++i) orow[i] = __float2bfloat16_rn(acc[i][j]);
+        for (int i = 0; i < NPW; ++i) orow[i] = __float2bfloat16_rn(WT ? acc[i][j] * sc[i] : acc[i][j]);
       }
     }
   }
@@ -207,15 +235,18 @@ constexpr int kTailCols = 4;
 constexpr int kTailSteps = 4;
 constexpr int kTailSlots = kGemvThreads / 32;   // one warp per slot
 
+template <int WT>
 __global__ void __launch_bounds__(kGemvThreads)
-    down_combine_gemv_kernel(const __nv_bfloat16* __restrict__ h, const __nv_bfloat16* __restrict__ w,
-                             const int32_t* __restrict__ offsets, int G, int rows, int N, int K, int k,
+    down_combine_gemv_kernel(const __nv_bfloat16* __restrict__ h, const uint8_t* __restrict__ w,
+                             const float* __restrict__ wscale, const int32_t* __restrict__ offsets, int G, int rows,
+                             int N, int K, int k,
                              const int32_t* __restrict__ inv_perm, const float* __restrict__ topk_w,
                              const __nv_bfloat16* __restrict__ shared, __nv_bfloat16* __restrict__ out,
                              int* status) {
   __shared__ int s_group[kTailSlots];            // group holding row r (rows <= k), or -1
   __shared__ float s_y[kTailSlots][kTailCols];   // y_j[n], bf16-rounded
   __shared__ int s_live[kTailSlots];
+  using WC = WeightChunk<WT>;
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -238,17 +269,17 @@ __global__ void __launch_bounds__(kGemvThreads)
     for (int c = 0; c < kTailCols; ++c) acc[c] = 0.f;
     if (g >= 0) {
       const __nv_bfloat16* hr = h + static_cast<size_t>(r) * K;
-      const __nv_bfloat16* wr = w + (static_cast<size_t>(g) * N + n0) * K;
+      const uint8_t* wr = w + (static_cast<size_t>(g) * N + n0) * K * WC::kBytes;
       for (int kb = lane * 8; kb < K; kb += 256 * kTailSteps) {
-        uint4 wv[kTailSteps][kTailCols], hv[kTailSteps];
+        typename WC::Vec wv[kTailSteps][kTailCols];
+        uint4 hv[kTailSteps];
 #pragma unroll
         for (int u = 0; u < kTailSteps; ++u) {
           const int k0 = kb + u * 256;
           if (k0 < K) {
             hv[u] = __ldg(reinterpret_cast<const uint4*>(hr + k0));
 #pragma unroll
-            for (int c = 0; c < kTailCols; ++c)
-              wv[u][c] = __ldg(reinterpret_cast<const uint4*>(wr + static_cast<size_t>(c) * K + k0));
+            for (int c = 0; c < kTailCols; ++c) wv[u][c] = WC::load(wr + static_cast<size_t>(c) * K * WC::kBytes, k0);
           }
         }
 #pragma unroll
@@ -259,7 +290,7 @@ __global__ void __launch_bounds__(kGemvThreads)
 #pragma unroll
           for (int c = 0; c < kTailCols; ++c) {
             float wf[8];
-            bf16x8(wv[u][c], wf);
+            WC::to_f32(wv[u][c], wf);
             float s = acc[c];
 #pragma unroll
             for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
@@ -275,7 +306,10 @@ __global__ void __launch_bounds__(kGemvThreads)
     if (lane == 0) {
       s_live[j] = g >= 0;
 #pragma unroll
-      for (int c = 0; c < kTailCols; ++c) s_y[j][c] = __bfloat162float(__float2bfloat16_rn(acc[c]));
+      for (int c = 0; c < kTailCols; ++c) {
+        const float v = WT && g >= 0 ? acc[c] * __ldg(wscale + static_cast<size_t>(g) * N + n0 + c) : acc[c];
+        s_y[j][c] = __bfloat162float(__float2bfloat16_rn(v));
+      }
     }
   }
   __syncthreads();
@@ -295,15 +329,15 @@ bool down_combine_gemv_applies(int G, int N, int K, int k) {
   return k <= kTailSlots && N % kTailCols == 0 && grouped_gemv_applies(G, N, K, 0, 1);
 }
 
-int down_combine_gemv_launch(const void* h, const void* w_down, const int32_t* offsets, int G, int N, int K, int k,
-                             const int32_t* inv_perm, const float* topk_w, const void* shared, void* out,
-                             int* status, cudaStream_t stream, int* launches) {
+int down_combine_gemv_launch(const void* h, const void* w_down, const float* w_scale, const int32_t* offsets, int G,
+                             int N, int K, int k, const int32_t* inv_perm, const float* topk_w, const void* shared,
+                             void* out, int* status, cudaStream_t stream, int* launches) {
   if (k < 1 || k > kTailSlots || N % kTailCols) return MOE_ERR_UNSUPPORTED;
   const dim3 g(N / kTailCols), b(kGemvThreads);
   const cudaError_t rc = launch_chained(
-      down_combine_gemv_kernel, g, b, 0, stream, static_cast<const __nv_bfloat16*>(h),
-      static_cast<const __nv_bfloat16*>(w_down), offsets, G, k, N, K, k, inv_perm, topk_w,
-      static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(out), status);
+      w_scale ? down_combine_gemv_kernel<1> : down_combine_gemv_kernel<0>, g, b, 0, stream,
+      static_cast<const __nv_bfloat16*>(h), static_cast<const uint8_t*>(w_down), w_scale, offsets, G, k, N, K, k,
+      inv_perm, topk_w, static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(out), status);
   if (rc != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
@@ -313,31 +347,37 @@ bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows) {
   return max_group_rows == 1 && G <= kMaxGemvGroups && K % 8 == 0 && (act == 1 || N % kRowsDown == 0);
 }
 
-int grouped_gemv_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
-                        int act, void* out, int* status, cudaStream_t stream, int* launches,
-                        const int32_t* a_rows, int a_src_rows, int max_group_rows, int grid_cap) {
+int grouped_gemv_launch(const void* a, const void* w, const float* w_scale, const int32_t* offsets, int G,
+                        int rows_max, int N, int K, int act, void* out, int* status, cudaStream_t stream,
+                        int* launches, const int32_t* a_rows, int a_src_rows, int max_group_rows, int grid_cap) {
   if (rows_max == 0) return MOE_OK;
   // at most min(G, rows_max) non-empty groups
   const long long groups = G < rows_max ? G : rows_max;
   const long long items = groups * (act == 1 ? N : N / kRowsDown);
   if (max_group_rows != 1) return MOE_ERR_UNSUPPORTED;
-  auto kernel = act == 1 ? grouped_gemv_kernel<1, 1> : grouped_gemv_kernel<0, 1>;
+  const int form = (act == 1 ? 1 : 0) + (w_scale ? 2 : 0);
+  auto kernel = form == 0 ? grouped_gemv_kernel<0, 1, 0>
+                          : form == 1 ? grouped_gemv_kernel<1, 1, 0>
+                                      : form == 2 ? grouped_gemv_kernel<0, 1, 1> : grouped_gemv_kernel<1, 1, 1>;
   // persistent: no more CTAs than stay resident (each lists the groups once)
   long long grid = (items + kGemvThreads / 32 - 1) / (kGemvThreads / 32);
   int* dev_status = nullptr;
   int sms = 0;
-  static int occupancy[2] = {0, 0};   // resident CTAs per SM of each form (looked up once)
-  int& per_sm = occupancy[act == 1];
+  static std::atomic<int> occupancy[4] = {};   // resident CTAs per SM of each form (looked up once)
   if (current_device_info(&dev_status, &sms) != MOE_OK) return MOE_ERR_CUDA;
-  if (per_sm == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kGemvThreads, 0) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  int per_sm = occupancy[form].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kGemvThreads, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    occupancy[form].store(per_sm, std::memory_order_relaxed);
+  }
   // resident CTAs of the SMs the launch may fill
   const long long resident = static_cast<long long>(grid_cap > 0 && grid_cap < sms ? grid_cap : sms) *
                              (per_sm > 0 ? per_sm : 1);
   if (grid > resident) grid = resident;
   const dim3 g(static_cast<unsigned>(grid)), b(kGemvThreads);
   const cudaError_t rc = launch_chained(kernel, g, b, 0, stream, static_cast<const __nv_bfloat16*>(a),
-                                        static_cast<const __nv_bfloat16*>(w), offsets, G, rows_max, N, K, a_rows,
+                                        static_cast<const uint8_t*>(w), w_scale, offsets, G, rows_max, N, K, a_rows,
                                         a_src_rows, static_cast<__nv_bfloat16*>(out), status);
   if (rc != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;

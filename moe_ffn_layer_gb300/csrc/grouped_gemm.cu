@@ -55,7 +55,6 @@ namespace moe {
 namespace {
 
 constexpr int kBK = 64;            // K per stage: one 128-byte swizzle row of bf16
-constexpr int kThreads = 192;      // 6 warps
 constexpr int kMaxGroups = 1024;
 constexpr int kTileRows128 = 128 * kBK * 2;   // bytes of a 128-row K block
 constexpr int kSmemBudget = 216 * 1024;
@@ -70,23 +69,41 @@ constexpr int tmem_cols_pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 
 // weight block (each CTA loads its own token rows and half of the weights);
 // an odd last tile is shared by two adjacent weight blocks instead (each CTA
 // loads its own weights and 64 of the tile's token rows).
-template <int SWAP, int W, int ACT, int MC = 0>
+//
+// WT = 1 (weights-on-M only): the weights are e4m3 codes with one fp32 scale
+// per weight row.  The producer streams the 8-bit weight tiles into their own
+// deep ring (the bytes in flight from HBM); four converter warps turn each
+// into the bf16 operand tile of a two-stage operand ring (exact: every e4m3
+// value is a bf16 value) and load the token tile beside it; the epilogue
+// multiplies each accumulator row by its scale.
+template <int SWAP, int W, int ACT, int MC = 0, int WT = 0>
 struct Cfg {
+  static constexpr int kThreads = WT ? 320 : 192;                          // 6 warps (+ 4 converter warps)
   static constexpr int kUnitRows = SWAP ? W : 128;                          // token rows per unit
   static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;
   static constexpr int kBBytes = W * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = kSmemBudget / kStageBytes;
+  static constexpr int kStages = WT ? 2 : kSmemBudget / kStageBytes;       // operand stages
+  static constexpr int k8Bytes = WT ? (ACT == 1 ? 2 : 1) * 128 * kBK : 0;  // 8-bit weights of a K block
+  static constexpr int k8Stages = WT ? (kSmemBudget - kStages * kStageBytes) / k8Bytes : 0;
+  static constexpr int kRingBytes = kStages * kStageBytes + k8Stages * k8Bytes;
   static constexpr int kOutCols = SWAP ? 128 : (ACT == 1 ? W / 2 : W);           // output columns per unit
   static constexpr int kAccCols = SWAP ? (ACT == 1 ? 2 : 1) * W : W;             // TMEM columns per unit
   static constexpr int kNumAcc = 2 * kAccCols <= 512 ? 2 : 1;
   static constexpr int kTmemCols = tmem_cols_pow2(kNumAcc * kAccCols);
-  // after the ring: the mbarriers (full/empty per stage, 2 tfull, 2 tempty,
-  // done), the TMEM slot, the abort flag, the unit total and 8 split words
-  static constexpr int kCtrlUsed = (2 * kStages + 5) * 8 + 4 + 4 + 4 + 8 * 4;
+  // after the rings: the mbarriers (full/empty per stage, 2 tfull, 2 tempty,
+  // done; with WT full/empty per 8-bit stage and a token barrier per operand
+  // stage), the TMEM slot, the abort flag, the unit total and 8 split words
+  static constexpr int kCtrlUsed = (2 * kStages + 5 + 2 * k8Stages + (WT ? kStages : 0)) * 8 + 4 + 4 + 4 + 8 * 4;
   static constexpr int kCtrlBytes = (kCtrlUsed + 127) / 128 * 128;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtrlBytes + 2 * (kMaxGroups + 1) * 4 + 128 * 4;
+  // the carve, from the 1024-aligned base: operand ring | 8-bit ring | control | group arrays
+  static constexpr int kOffW8 = kStages * kStageBytes;
+  static constexpr int kOffCtrl = kRingBytes;
+  static constexpr int kOffArrays = kRingBytes + kCtrlBytes;
+  static constexpr int kArrayBytes = 2 * (kMaxGroups + 1) * 4 + 128 * 4;
+  static constexpr int kSmemBytes = 1024 + kOffArrays + kArrayBytes;
   static_assert(kStages >= 2, "ring too shallow");
+  static_assert(!WT || (SWAP && !MC && k8Stages >= 4), "8-bit weights: weights-on-M, a deep 8-bit ring");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -112,6 +129,7 @@ struct GemmArgs {
   const int32_t* a_rows;   // non-null: token row r is row a_rows[r] of the token tensor
                            // (fetched with TMA gather4; no permuted copy needed)
   uint64_t wait_ns;        // limit of every bounded wait but the drains (0: expire at once)
+  const float* wscale;     // 8-bit weights: one scale per weight row ([G][rows of W[g]])
 };
 
 // fp32 values one TMEM lane keeps per split-K partial
@@ -189,28 +207,33 @@ struct WorkIter {
 // last arriver's sum), in K blocks; measured on decode shapes.
 constexpr int kPieceCost = 6;
 
-template <int SWAP, int W, int ACT, int MC = 0>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int SWAP, int W, int ACT, int MC = 0, int WT = 0>
+__global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_wgt,
                         const GemmArgs args) {
   static_assert(!MC || (!SWAP && W == 256 && (ACT == 0 || ACT == 1)), "pairs: tokens-on-M, 256-wide blocks");
   constexpr int kTokHalf = 64 * kBK * 2;   // bytes of 64 token rows of a K block
-  using C = Cfg<SWAP, W, ACT, MC>;
+  using C = Cfg<SWAP, W, ACT, MC, WT>;
+  constexpr int kThreads = C::kThreads;
   constexpr uint16_t kPairMask = 0x3;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint8_t* w8_base = smem + C::kOffW8;               // 8-bit weight ring (WT)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffCtrl);
   uint64_t* full_bar = bars;                        // [kStages]
   uint64_t* empty_bar = bars + C::kStages;          // [kStages]
   uint64_t* tfull_bar = bars + 2 * C::kStages;      // [2]
   uint64_t* tempty_bar = tfull_bar + 2;             // [2]
   uint64_t* done_bar = tempty_bar + 2;              // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  uint64_t* w8full_bar = done_bar + 1;              // [k8Stages]: 8-bit tile landed
+  uint64_t* w8empty_bar = w8full_bar + C::k8Stages; // [k8Stages]: converted
+  uint64_t* tok_bar = w8empty_bar + C::k8Stages;    // [kStages]: token tile of an operand stage landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tok_bar + (WT ? C::kStages : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] mode, [1] last arriver, [2..5] warp ok, [6] P, [7] S
-  int* s_off = reinterpret_cast<int*>(smem + C::kStages * C::kStageBytes + C::kCtrlBytes);   // [G+1]
+  int* s_off = reinterpret_cast<int*>(smem + C::kOffArrays);                       // [G+1]
   int* s_ustart = s_off + (kMaxGroups + 1);                                          // [G+1]
   int* s_gidx = s_ustart + (kMaxGroups + 1);                                         // [128] gathered rows
 
@@ -224,7 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1 && lane == 0) {
     // with pairs a stage is free once both CTAs' MMAs are done with it (the
     // peer's multicast writes into this CTA's copy too)
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], MC ? 2 : 1); }
+    // (WT: an operand stage is full once the four converter warps have written it)
+    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full_bar[s], WT ? 4 : 1); mbar_init(&empty_bar[s], MC ? 2 : 1); }
+    if (WT) {
+      for (int s = 0; s < C::k8Stages; ++s) { mbar_init(&w8full_bar[s], 1); mbar_init(&w8empty_bar[s], 4); }
+      for (int s = 0; s < C::kStages; ++s) mbar_init(&tok_bar[s], 1);
+    }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
     mbar_init(done_bar, 1);
     fence_barrier_init();
@@ -361,7 +389,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int wrows = ACT == 1 ? 2 * args.N : args.N;   // weight rows per group
 
-  if (warp == 0) {
+  if (warp == 0 && WT) {
+    // ------------------------------------------------------------ 8-bit weight producer
+    // lane 0 streams the e4m3 weight tiles (gate and up, or the plain rows;
+    // 128 rows x 64 codes each) into the 8-bit ring, as deep as it goes; the
+    // converter warps take them from there
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      long long issued = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
+      Piece pc;
+      while (ok && wi.next(pc)) {
+        int g, row0, nrows, wb, kind;
+        decode(pc.u, g, row0, nrows, wb, kind);
+        const int wrow = g * wrows + wb * C::kOutCols;
+        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
+          if (!mbar_wait(&w8empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+          uint8_t* dst = w8_base + stage * C::k8Bytes;
+          mbar_arrive_expect_tx(&w8full_bar[stage], C::k8Bytes);
+          tma_load_2d(dst, &tm_wgt, &w8full_bar[stage], kb * kBK, wrow, pol_w);
+          if (ACT == 1) tma_load_2d(dst + 128 * kBK, &tm_wgt, &w8full_bar[stage], kb * kBK, wrow + args.N, pol_w);
+          ++issued;
+          if (++stage == C::k8Stages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // drain: every tile issued has landed before the CTA may exit
+      for (int s = 0; s < C::k8Stages; ++s) {
+        const long long fills = issued / C::k8Stages + (s < issued % C::k8Stages ? 1 : 0);
+        if (fills > 0) mbar_wait_timed(&w8full_bar[s], static_cast<uint32_t>((fills - 1) & 1), args.status);
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // lane 0 issues the copies; with gathered rows the whole warp first
     // stages the unit's source row indices in shared memory
@@ -484,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int kb = kb0; kb < pc.kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+          if (WT && !mbar_wait(&tok_bar[stage], phase, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * C::kStageBytes);
           const uint32_t sb = sa + C::kABytes;
@@ -519,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(done_bar);
       mbar_wait_timed(done_bar, 0, args.status);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                    // TMEM lane quadrant of this warp
     const int lrow = q * 32 + lane;            // TMEM lane = accumulator row
@@ -552,6 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // accumulator row = output column wb*128 + lrow; accumulator column =
         // token, chain c of gate (h = 0) / up (h = 1) at column (h*C + c)*cw
         __nv_bfloat16* ocol = args.out + static_cast<size_t>(row0) * args.N + wb * 128 + lrow;
+        // 8-bit weights: this accumulator row's scales (gate and up rows, or the row)
+        float sg_scale = 1.f, su_scale = 1.f;
+        if (WT) {
+          const size_t wr0 = static_cast<size_t>(g) * wrows + wb * 128 + lrow;
+          sg_scale = __ldg(args.wscale + wr0);
+          if (ACT == 1) su_scale = __ldg(args.wscale + wr0 + args.N);
+        }
+        auto out_value = [&](float gv, float uv) {
+          if (WT) { gv *= sg_scale; uv *= su_scale; }
+          return ACT == 1 ? gv / (1.0f + __expf(-gv)) * uv : gv;
+        };
         const int n16 = (nrows + 15) >> 4;
         const int chains = swap_chains(n16, C::kAccCols, ACT == 1);
         const int cw = n16 * 16;
@@ -584,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               if (j * 16 + i < nrows) {
-                const float h = ACT == 1 ? gs[i] / (1.0f + __expf(-gs[i])) * us[i] : gs[i];
+                const float h = out_value(gs[i], us[i]);
                 ocol[static_cast<size_t>(j * 16 + i) * args.N] = __float2bfloat16_rn(h);
               }
             }
@@ -651,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kSplitRows; ++i) {
               if (i < nrows) {
-                const float h = ACT == 1 ? gs[i] / (1.0f + __expf(-gs[i])) * us[i] : gs[i];
+                const float h = out_value(gs[i], us[i]);
                 ocol[static_cast<size_t>(i) * args.N] = __float2bfloat16_rn(h);
               }
             }
@@ -717,6 +790,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_acc();
       }
     }
+  } else if constexpr (WT) {
+    // ------------------------------------------------------------ converters
+    // warps 6..9: an 8-bit weight stage -> the bf16 operand tile(s) of an
+    // operand stage, in the 128-byte swizzle the MMA reads (the 16-byte chunk
+    // c of row r lands at chunk c ^ (r & 7) of the row); converter warp 0 also
+    // loads the stage's token tile.  A stage is full when all four warps have
+    // written it (their writes fenced for the async proxy) and its token tile
+    // has landed.
+    const int cw = warp - 6;
+    const int ct = threadIdx.x - 192;
+    const uint64_t pol_tok = l2_policy_evict_last();
+    int stage = 0, s8 = 0;
+    uint32_t phase = 0, ph8 = 0;
+    long long tok_issued = 0;
+    bool ok = true;
+    WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
+    Piece pc;
+    while (ok && wi.next(pc)) {
+      int g, row0, nrows, wb, kind;
+      decode(pc.u, g, row0, nrows, wb, kind);
+      const int n16 = (nrows + 15) >> 4;
+      const int nfetch = n16 * 16;
+      if (args.a_rows && cw == 0) {
+        __syncwarp();
+        for (int i = lane; i < nfetch; i += 32) s_gidx[i] = args.a_rows[row0 + min(i, nrows - 1)];
+        __syncwarp();
+      }
+      for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&w8full_bar[s8], ph8, abort_flag, args.status, args.wait_ns));
+        if (ok)
+          ok = __all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns));
+        if (!ok) break;
+        uint8_t* sa = stage_base + stage * C::kStageBytes;
+        if (cw == 0 && lane == 0) {
+          const int kc = kb * kBK;
+          uint8_t* stok = sa + C::kABytes;
+          mbar_arrive_expect_tx(&tok_bar[stage], static_cast<uint32_t>(nfetch * kBK * 2));
+          if (args.a_rows) {
+            for (int j = 0; j < nfetch; j += 4)
+              tma_gather4(stok + j * kBK * 2, &tm_tok, &tok_bar[stage], kc, s_gidx[j], s_gidx[j + 1], s_gidx[j + 2],
+                          s_gidx[j + 3], pol_tok);
+          } else {
+            for (int j = 0; j < n16; ++j)
+              tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &tok_bar[stage], kc, row0 + 16 * j, pol_tok);
+          }
+          ++tok_issued;
+        }
+        const uint8_t* src = w8_base + s8 * C::k8Bytes;
+        constexpr int kChunks = C::k8Bytes / 8;   // 8 codes each: tile, row, 16-byte chunk of the bf16 row
+#pragma unroll 4
+        for (int i = ct; i < kChunks; i += 128) {
+          const int tile = i >> 10, r = (i >> 3) & 127, c = i & 7;
+          const uint2 v = *reinterpret_cast<const uint2*>(src + i * 8);
+          const uint4 o = make_uint4(e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y),
+                                     e4m3x2_to_bf16x2(v.y >> 16));
+          *reinterpret_cast<uint4*>(sa + tile * kTileRows128 + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&full_bar[stage]);
+          mbar_arrive(&w8empty_bar[s8]);
+        }
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        if (++s8 == C::k8Stages) { s8 = 0; ph8 ^= 1u; }
+      }
+    }
+    if (cw == 0 && lane == 0) {
+      // drain: every token tile issued has landed before the CTA may exit
+      for (int s = 0; s < C::kStages; ++s) {
+        const long long fills = tok_issued / C::kStages + (s < tok_issued % C::kStages ? 1 : 0);
+        if (fills > 0) mbar_wait_timed(&tok_bar[s], static_cast<uint32_t>((fills - 1) & 1), args.status);
+      }
+    }
   }
 
   tc_fence_before();
@@ -762,6 +909,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte tensor [rows][cols] (e4m3 weights), box [box_rows][64 bytes], no
+// swizzle (the converter warps read it row by row).
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Split-K scratch of one weights-on-M launch: a ticket counter per unit and
 // fp32 partial slots (at most kMaxSlots sub-units).
 struct SplitPlan {
@@ -792,12 +953,14 @@ SplitPlan split_plan(int G, int rows_max, int N, int act, int max_slots = kMaxSl
   return p;
 }
 
-template <int SWAP, int W, int ACT, int MC = 0>
+template <int SWAP, int W, int ACT, int MC = 0, int WT = 0>
 int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K, void* out,
                int* status, const GemmScratch* scratch, int grid_cap, cudaStream_t stream, int* launches,
-               int max_slots = kMaxSlots, int K_a = 0, const int32_t* a_rows = nullptr, int a_src_rows = 0) {
-  using C = Cfg<SWAP, W, ACT, MC>;
-  auto kernel = grouped_gemm_kernel<SWAP, W, ACT, MC>;
+               int max_slots = kMaxSlots, int K_a = 0, const int32_t* a_rows = nullptr, int a_src_rows = 0,
+               const float* w_scale = nullptr) {
+  using C = Cfg<SWAP, W, ACT, MC, WT>;
+  constexpr int kThreads = C::kThreads;
+  auto kernel = grouped_gemm_kernel<SWAP, W, ACT, MC, WT>;
   // per device: the shared-memory attribute set once, the pairs that fit at once
   static bool attr_done[64] = {};
   static int max_clusters[64] = {};
@@ -840,13 +1003,15 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   } else if (!make_map(&tt, a, static_cast<uint64_t>(rows_max), static_cast<uint64_t>(K_a ? K_a : K), tok_box)) {
     return MOE_ERR_CUDA;
   }
-  if (!make_map(&tw, w, static_cast<uint64_t>(G) * wrows, static_cast<uint64_t>(K), wgt_box)) return MOE_ERR_CUDA;
+  if (WT ? !make_map_u8(&tw, w, static_cast<uint64_t>(G) * wrows, static_cast<uint64_t>(K), wgt_box)
+         : !make_map(&tw, w, static_cast<uint64_t>(G) * wrows, static_cast<uint64_t>(K), wgt_box))
+    return MOE_ERR_CUDA;
   // upper bound on the unit count: every non-empty group adds at most one partial row block
   const long long nonempty = offsets ? (G < rows_max ? G : rows_max) : 1;
   long long bound = (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) *
                     (N / C::kOutCols / (MC ? 2 : 1));
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
-                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows, wait_limit_ns()};
+                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows, wait_limit_ns(), w_scale};
   if (SWAP && scratch && scratch->counters && scratch->partials) {
     const SplitPlan p = split_plan(G, rows_max, N, ACT, max_slots);
     if (p.partial_bytes && scratch->partial_bytes >= p.partial_bytes) {
@@ -915,14 +1080,24 @@ GemmScratch grouped_gemm_scratch(void* ws, size_t ws_bytes) {
 
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, const GemmScratch* scratch, int grid_cap, cudaStream_t stream,
-                        int* launches, const int32_t* a_rows, int a_src_rows, int max_slots, int max_group_rows) {
+                        int* launches, const int32_t* a_rows, int a_src_rows, int max_slots, int max_group_rows,
+                        const float* w_scale) {
   if (rows_max == 0) return MOE_OK;
   if (max_slots <= 0) max_slots = kMaxSlots;
   // groups of one row: a weight stream on the CUDA cores
   const int bound = rows_max == 1 ? 1 : max_group_rows;
   if (act != 2 && grouped_gemv_applies(G, N, K, act, bound))
-    return grouped_gemv_launch(a, w, offsets, G, rows_max, N, K, act, out, status, stream, launches, a_rows,
+    return grouped_gemv_launch(a, w, w_scale, offsets, G, rows_max, N, K, act, out, status, stream, launches, a_rows,
                                a_src_rows, bound, grid_cap);
+  if (w_scale) {
+    // 8-bit weights: the weights-on-M form only (decode-sized batches)
+    if (!grouped_gemm_weights_on_m(G, rows_max, N) || act == 2) return MOE_ERR_UNSUPPORTED;
+    if (act == 1)
+      return launch_cfg<1, kSwapRows, 1, 0, 1>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap,
+                                               stream, launches, max_slots, 0, a_rows, a_src_rows, w_scale);
+    return launch_cfg<1, kSwapRows, 0, 0, 1>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,
+                                             launches, max_slots, 0, a_rows, a_src_rows, w_scale);
+  }
   if (grouped_gemm_weights_on_m(G, rows_max, N)) {
     if (act == 1)
       return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,

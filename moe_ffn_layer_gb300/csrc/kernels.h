@@ -52,27 +52,30 @@ GemmScratch grouped_gemm_scratch(void* ws, size_t ws_bytes);
 // a_rows (nullable): token row r of the product is row a_rows[r] of `a`, a
 // [a_src_rows][K] tensor (rows fetched by TMA gather4, no permuted copy).
 // max_group_rows (0: unknown): a bound on any group's rows that the caller knows.
+// w_scale (nullable): w holds e4m3 codes with one fp32 scale per weight row
+// (weights-on-M shapes and one-row groups only; others MOE_ERR_UNSUPPORTED).
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, const GemmScratch* scratch, int grid_cap,
                         cudaStream_t stream, int* launches, const int32_t* a_rows = nullptr, int a_src_rows = 0,
-                        int max_slots = 0, int max_group_rows = 0);
+                        int max_slots = 0, int max_group_rows = 0, const float* w_scale = nullptr);
 int grouped_gemm_max_groups();
 // Groups of one row (max_group_rows: a bound the caller knows, e.g. T when a
 // token adds at most one row per group) run on the CUDA cores: a weight stream
 // where a tensor-core tile would mostly hold padding.
 bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows);
+// w_scale non-null: w holds e4m3 codes with one fp32 scale per weight row.
 // grid_cap: SMs the launch may fill (0: all).
-int grouped_gemv_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
-                        int act, void* out, int* status, cudaStream_t stream, int* launches, const int32_t* a_rows,
-                        int a_src_rows, int max_group_rows, int grid_cap = 0);
+int grouped_gemv_launch(const void* a, const void* w, const float* w_scale, const int32_t* offsets, int G,
+                        int rows_max, int N, int K, int act, void* out, int* status, cudaStream_t stream,
+                        int* launches, const int32_t* a_rows, int a_src_rows, int max_group_rows, int grid_cap = 0);
 // One token: gmm2 over its k one-row groups and the combine in one launch
 // (out[H] = bf16(sum_j topk_w[j] * y_j + shared)), the same bits as the one-row
 // gmm2 followed by combine_launch.  h: [k][K] rows in group order; shared
 // nullable.  k <= 8.
 bool down_combine_gemv_applies(int G, int N, int K, int k);
-int down_combine_gemv_launch(const void* h, const void* w_down, const int32_t* offsets, int G, int N, int K, int k,
-                             const int32_t* inv_perm, const float* topk_w, const void* shared, void* out,
-                             int* status, cudaStream_t stream, int* launches);
+int down_combine_gemv_launch(const void* h, const void* w_down, const float* w_scale, const int32_t* offsets, int G,
+                             int N, int K, int k, const int32_t* inv_perm, const float* topk_w, const void* shared,
+                             void* out, int* status, cudaStream_t stream, int* launches);
 // logits[T][E] fp32 = x[T][H] . (hi + mid + lo)^T with wr3 = bf16 [E][3H] holding
 // the three bf16 terms of the fp32 router weights in K order (hi | mid | lo);
 // the x tile is re-read for each of the three.  E % 64 == 0, H % 64 == 0.

@@ -21,16 +21,24 @@ class MoEFFN:
     """Weights (device tensors): w_router fp32 [E,H]; router_bias fp32 [E] or
     None; w_gate_up bf16 [E,2I,H]; w_down bf16 [E,H,I]; ws_gate_up bf16
     [2I_s,H] and ws_down bf16 [H,I_s], or None for a layer without a shared
-    expert."""
+    expert.  With s_gate_up fp32 [E,2I] and s_down fp32 [E,H] the routed
+    weights are e4m3 codes (uint8 tensors of the same shapes) with one scale
+    per weight row, and forward() calls moe_forward_w8."""
 
-    def __init__(self, k: int, w_router, router_bias, w_gate_up, w_down, ws_gate_up=None, ws_down=None):
+    def __init__(self, k: int, w_router, router_bias, w_gate_up, w_down, ws_gate_up=None, ws_down=None,
+                 s_gate_up=None, s_down=None):
         E, twoI, H = w_gate_up.shape
         I_s = 0 if ws_gate_up is None else ws_gate_up.shape[0] // 2
         self.H, self.E, self.k, self.I, self.I_s = H, E, k, twoI // 2, I_s
         self.device = w_gate_up.device
         self.tensors = (w_router, router_bias, w_gate_up, w_down, ws_gate_up, ws_down)
+        self.scales = None if s_gate_up is None else (s_gate_up, s_down)
         self.dims = B.moe_dims(H, E, k, twoI // 2, I_s)
-        self.weights = B.moe_weights(*(B.ptr(t) for t in self.tensors))
+        if self.scales is None:
+            self.weights = B.moe_weights(*(B.ptr(t) for t in self.tensors))
+        else:
+            self.weights = B.moe_weights_w8(*(B.ptr(t) for t in (w_router, router_bias, w_gate_up, s_gate_up, w_down,
+                                                                 s_down, ws_gate_up, ws_down)))
         self.side = torch.cuda.Stream(self.device)
         self.ev_fork = torch.cuda.Event()
         self.ev_join = torch.cuda.Event()
@@ -42,9 +50,15 @@ class MoEFFN:
 
     @classmethod
     def from_inputs(cls, inp: dict, k: int, device="cuda") -> "MoEFFN":
-        """From the numpy arrays of ``synth.make_inputs`` (bf16 as uint16 bits)."""
+        """From the numpy arrays of ``synth.make_inputs`` (bf16 as uint16 bits)
+        or ``synth.make_inputs_w8`` (e4m3 codes as uint8 with row scales)."""
         f32 = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
         b16 = lambda a: None if a is None else bf16_tensor(a, device)
+        if "w_gate_up_scale" in inp:
+            u8 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.uint8)).to(device)
+            return cls(k, f32(inp["w_router"]), f32(inp["bias"]), u8(inp["w_gate_up"]), u8(inp["w_down"]),
+                       b16(inp["ws_gate_up"]), b16(inp["ws_down"]), f32(inp["w_gate_up_scale"]),
+                       f32(inp["w_down_scale"]))
         return cls(k, f32(inp["w_router"]), f32(inp["bias"]), b16(inp["w_gate_up"]), b16(inp["w_down"]),
                    b16(inp["ws_gate_up"]), b16(inp["ws_down"]))
 
@@ -67,8 +81,8 @@ class MoEFFN:
             out = torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device)
         stream = stream if stream is not None else torch.cuda.current_stream(self.device)
         ws = self.workspace(T)
-        B.moe_forward(self.dims, self.weights, x, T, out, ws, ws.numel(), stream, self.side, self.ev_fork,
-                      self.ev_join)
+        call = B.moe_forward if self.scales is None else B.moe_forward_w8
+        call(self.dims, self.weights, x, T, out, ws, ws.numel(), stream, self.side, self.ev_fork, self.ev_join)
         return out
 
     __call__ = forward

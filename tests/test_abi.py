@@ -130,6 +130,20 @@ def test_host_side_argument_checks(lib):
                          None) == 0
 
 
+def test_w8_calls_refuse_shapes_outside_the_weight_stream(lib):
+    """FP8 weights serve the weights-on-M (decode-sized) shapes: larger batches
+    are refused on the host, before anything is launched."""
+    fake = 1 << 20
+    # 300 rows over 2 groups: more than 64 rows per group -> tokens-on-M
+    assert _rc(B.moe_grouped_gemm_w8, fake, fake, fake, fake, 2, 300, 256, 128, 1, fake, None, 0, None) == -2
+    assert _rc(B.moe_grouped_gemm_w8, fake, fake, None, fake, 2, 64, 256, 128, 1, fake, None, 0, None) == -1
+    d = B.moe_dims(2048, 128, 8, 768, 2048)
+    w8 = B.moe_weights_w8(fake, None, fake, fake, fake, fake, fake, fake)
+    assert _rc(B.moe_forward_w8, d, w8, fake, 8192, fake, fake, 1 << 40, fake, fake, fake, fake) == -2   # prefill
+    no_scales = B.moe_weights_w8(fake, None, fake, None, fake, None, fake, fake)
+    assert _rc(B.moe_forward_w8, d, no_scales, fake, 8, fake, fake, 1 << 30, fake, fake, fake, fake) == -1
+
+
 def test_missing_library_is_an_error(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "_lib", None)
     monkeypatch.setattr(B, "library_path", lambda: str(tmp_path / "absent.so"))
