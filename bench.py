@@ -52,7 +52,10 @@ L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # every shape of the metric, timed after the headline unless --no-sweep
 SWEEP = [("decode", 1), ("decode", 4), ("decode", 8), ("batched_decode", 64), ("batched_decode", 256),
-         ("prefill", 8192), ("large_prefill", 16384)]
+         ("prefill", 8192), ("large_prefill", 16384),
+         # the same decode shapes with FP8 (e4m3, per-row scales) routed expert weights
+         ("decode_w8", 1), ("decode_w8", 4), ("decode_w8", 8), ("batched_decode_w8", 64),
+         ("batched_decode_w8", 256)]
 SWEEP_SECONDS = 0.25          # timed replays per sweep workload
 ONE_GPU = ("one GPU only: the layer does not shard, and its prefill matmuls share operand tiles between the two "
            "CTAs of a cluster by TMA multicast, which stays inside one GPU's own memory")
@@ -68,11 +71,22 @@ def peaks():
 
 # ---------------------------------------------------------------- algorithmic units
 
+def is_w8(w) -> bool:
+    """A workload with FP8 (e4m3) routed expert weights (per-row fp32 scales)."""
+    return w.name.split("@")[0].endswith("_w8")
+
+
+def expert_bytes(w) -> int:
+    """Bytes of one routed expert's weights: 3 I H elements (2 or 1 bytes each)
+    plus, for FP8, one fp32 scale per weight row (2I + H rows)."""
+    return 3 * w.H * w.I + (2 * w.I + w.H) * 4 if is_w8(w) else 6 * w.H * w.I
+
+
 def layer_units(w, nonempty):
     """Algorithmic bytes and FLOPs of one layer forward (intermediates not
     counted): weights of every expert that received a token, the shared expert,
     the router, x and out; FLOPs of the routed and shared MLPs and the router."""
-    bytes_ = (6 * w.H * w.I * nonempty + 6 * w.H * w.Is + 4 * w.E * w.H + 2 * w.T * w.H * 2)
+    bytes_ = (expert_bytes(w) * nonempty + 6 * w.H * w.Is + 4 * w.E * w.H + 2 * w.T * w.H * 2)
     flops = 2 * w.T * w.k * 3 * w.H * w.I + 2 * w.T * 3 * w.H * w.Is + 2 * w.T * w.E * w.H
     return bytes_, flops
 
@@ -80,16 +94,17 @@ def layer_units(w, nonempty):
 def routed_units(w, nonempty):
     """The routed path alone (router, dispatch, both routed matmuls, combine):
     weights of the non-empty experts, the router weights, x and out."""
-    bytes_ = 6 * w.H * w.I * nonempty + 4 * w.E * w.H + 2 * w.T * w.H * 2
+    bytes_ = expert_bytes(w) * nonempty + 4 * w.E * w.H + 2 * w.T * w.H * 2
     flops = 2 * w.T * w.k * 3 * w.H * w.I + 2 * w.T * w.E * w.H
     return bytes_, flops
 
 
 def gate_up_units(w, nonempty):
     """gate_up GroupedMatmul: reads the 2I x H weights of each non-empty expert
-    and the T*k dispatched rows, writes T*k rows of h."""
+    (and their row scales, FP8) and the T*k dispatched rows, writes T*k rows of h."""
     rows = w.T * w.k
-    bytes_ = nonempty * 2 * w.I * w.H * 2 + rows * w.H * 2 + rows * w.I * 2
+    wb = nonempty * 2 * w.I * (w.H + 4) if is_w8(w) else nonempty * 2 * w.I * w.H * 2
+    bytes_ = wb + rows * w.H * 2 + rows * w.I * 2
     flops = 2 * rows * 2 * w.I * w.H
     return bytes_, flops
 
@@ -102,8 +117,7 @@ def tokens_per_s(tokens_per_step: int, steps: int, ms: float) -> float:
 def weight_copies(w) -> tuple[int, int]:
     """(R, touched bytes): R device copies of the expert weights, enough that R
     x the bytes one forward touches is at least 4 x L2."""
-    wgt_bytes = 3 * w.I * w.H * 2
-    touched = min(w.E, w.T * w.k) * wgt_bytes + 6 * w.H * w.Is
+    touched = min(w.E, w.T * w.k) * expert_bytes(w) + 6 * w.H * w.Is
     return int(min(16, max(2, -(-4 * L2_BYTES // max(touched, 1))))), touched
 
 
@@ -119,6 +133,8 @@ def config_of(w) -> dict:
     R, touched = weight_copies(w)
     return {"workload": f"{w.name.split('@')[0]} T={w.T}", "T": w.T, "H": w.H, "E": w.E, "k": w.k, "I": w.I,
             "I_s": w.Is, "routing": _routing_desc(w), "parallelism": "one GPU (the layer does not shard)",
+            "weights": ("routed experts e4m3 with per-row fp32 scales, shared expert bf16" if is_w8(w)
+                        else "bf16"),
             "l2": f"expert weights rotate over {R} device copies ({R} x {touched / 1e6:.0f} MB touched >= 4 x L2); "
                   f"one CUDA graph per copy, replayed back to back"}
 
@@ -216,11 +232,20 @@ class WeightBed:
         from moe_ffn_layer_gb300 import synth
         from moe_ffn_layer_gb300.layer import bf16_tensor
         self.dev = dev
-        wgu, wd = synth.make_expert_weights(w, seed)
         sgu, sd = synth.make_shared_weights(w, seed)
-        self.host = dict(w_gate_up=wgu, w_down=wd, ws_gate_up=sgu, ws_down=sd)
         b16 = lambda a: None if a is None else bf16_tensor(a, dev)
-        self.copies = [(b16(wgu), b16(wd), b16(sgu), b16(sd))]
+        if is_w8(w):
+            wgu, swgu, wd, swd = synth.make_expert_weights_w8(w, seed)
+            self.host = dict(w_gate_up=wgu, w_gate_up_scale=swgu, w_down=wd, w_down_scale=swd, ws_gate_up=sgu,
+                             ws_down=sd)
+            u8 = lambda a: torch.from_numpy(a).to(dev)
+            # (gate_up, down, shared gate_up, shared down, gate_up scales, down scales)
+            self.copies = [(u8(wgu), u8(wd), b16(sgu), b16(sd), torch.from_numpy(swgu).to(dev),
+                            torch.from_numpy(swd).to(dev))]
+        else:
+            wgu, wd = synth.make_expert_weights(w, seed)
+            self.host = dict(w_gate_up=wgu, w_down=wd, ws_gate_up=sgu, ws_down=sd)
+            self.copies = [(b16(wgu), b16(wd), b16(sgu), b16(sd))]
         self._torch = torch
 
     def get(self, R):
@@ -275,7 +300,7 @@ def measure(w, bed, args, clk, K, W, headline=False):
     if args.copies:
         R = args.copies
     copies = bed.get(R)
-    layers = [MoEFFN(w.k, wr, b, *c) for c in copies]
+    layers = [MoEFFN(w.k, wr, b, *c) for c in copies]   # (FP8 copies carry their scales last)
     outs = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
@@ -362,7 +387,7 @@ def dominant_kernel(w, copies, wr, b, x, offs, xperm, nonempty, pk, pk_src, stre
     R = len(copies)
     M = max(20, min(400, K))
     if w.T <= 16:
-        routed = [MoEFFN(w.k, wr, b, c[0], c[1], None, None) for c in copies]
+        routed = [MoEFFN(w.k, wr, b, c[0], c[1], None, None, *c[4:]) for c in copies]
         o = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=x.device)
         for L in routed:
             L.forward(x, o, stream)
@@ -383,9 +408,14 @@ def dominant_kernel(w, copies, wr, b, x, offs, xperm, nonempty, pk, pk_src, stre
         with torch.cuda.graph(g, stream=stream):
             cs = torch.cuda.current_stream()
             for i in range(M):
-                B.moe_grouped_gemm(xperm, copies[i % R][0], offs, w.E, w.T * w.k, w.I, w.H, 1, h, g_ws, gb_ws, cs)
+                if is_w8(w):
+                    B.moe_grouped_gemm_w8(xperm, copies[i % R][0], copies[i % R][4], offs, w.E, w.T * w.k, w.I, w.H,
+                                          1, h, g_ws, gb_ws, cs)
+                else:
+                    B.moe_grouped_gemm(xperm, copies[i % R][0], offs, w.E, w.T * w.k, w.I, w.H, 1, h, g_ws, gb_ws,
+                                       cs)
                 n_launch = B.moe_last_launch_count()
-        kernel = "grouped_gemm gate_up+SiLU*mul"
+        kernel = "grouped_gemm gate_up+SiLU*mul" + (" (e4m3 weights)" if is_w8(w) else "")
         gb, gf = gate_up_units(w, nonempty)
     with torch.cuda.stream(stream):
         g.replay()
@@ -449,7 +479,7 @@ def run_gpu(args, w):
     beds = {}
 
     def bed_for(wl):
-        key = (wl.H, wl.E, wl.I, wl.Is, wl.sigma_w)
+        key = (wl.H, wl.E, wl.I, wl.Is, wl.sigma_w, is_w8(wl))
         if key not in beds:
             if len(beds) >= 1:          # one set of weights on the device at a time
                 beds.clear()

@@ -358,11 +358,25 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   return __uint_as_float(((c & 0x7Fu) << 20) | ((c & 0x80u) << 24)) * 0x1p120f;
 }
 
-// The two e4m3 codes in bits 0..15 of w (bits 0..7 first) as a bf16 pair (the
-// first in the low half).  Every e4m3 value has at most four significant bits,
-// so the upper half of its f32 bits is its exact bf16 encoding.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w) {
-  return __byte_perm(__float_as_uint(e4m3_to_f32(w)), __float_as_uint(e4m3_to_f32(w >> 8)), 0x7632);
+// Four e4m3 codes (bytes 0..3 of v, in order) as two bf16 pairs: .x holds
+// codes 0 and 1, .y codes 2 and 3 (the first of each in the low half).  A
+// code's sign put at bit 15 of a 16-bit half and its exponent and mantissa at
+// bits 10..4 read as the bf16 2^(e-127) * 1.m, or the subnormal 0.m * 2^-126
+// for e = 0; one bf16 multiply by 2^120 moves the bias from 127 to 7, exactly
+// (every e4m3 value is a normal bf16).  The byte permute puts codes 0 and 1 in
+// the high bytes of the two halves, and codes 2 and 3 after a shift by 8.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t v) {
+  constexpr uint32_t kTwo120 = 0x7B807B80u;  // 2^120 in both halves
+  const uint32_t q = __byte_perm(v, 0u, 0x1302);  // bytes: code 2, code 0, code 3, code 1
+  const uint32_t r = q << 8;                      // codes 2 and 3 in the high bytes
+  const uint32_t x = (q & 0x80008000u) | ((q >> 4) & 0x07F007F0u);
+  const uint32_t y = (r & 0x80008000u) | ((r >> 4) & 0x07F007F0u);
+  return make_uint2(bf16x2_mul(x, kTwo120), bf16x2_mul(y, kTwo120));
 }
 
 // Eight e4m3 codes (v.x bytes 0..3, then v.y) as floats.

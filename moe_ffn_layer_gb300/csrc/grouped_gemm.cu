@@ -71,22 +71,25 @@ constexpr int tmem_cols_pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 
 // loads its own weights and 64 of the tile's token rows).
 //
 // WT = 1 (weights-on-M only): the weights are e4m3 codes with one fp32 scale
-// per weight row.  The producer streams the 8-bit weight tiles into their own
-// deep ring (the bytes in flight from HBM); four converter warps turn each
-// into the bf16 operand tile of a two-stage operand ring (exact: every e4m3
-// value is a bf16 value) and load the token tile beside it; the epilogue
+// per weight row.  The producer streams the 8-bit weight tiles and the token
+// tiles into their own rings (the bytes in flight from HBM); eight converter
+// warps turn each 8-bit tile into the bf16 operand tile of a two-stage
+// operand ring (exact: every e4m3 value is a bf16 value); the epilogue
 // multiplies each accumulator row by its scale.
+constexpr int kConvWarps = 8;
 template <int SWAP, int W, int ACT, int MC = 0, int WT = 0>
 struct Cfg {
-  static constexpr int kThreads = WT ? 320 : 192;                          // 6 warps (+ 4 converter warps)
+  static constexpr int kThreads = WT ? 192 + 32 * kConvWarps : 192;   // 6 warps (+ the converter warps)
   static constexpr int kUnitRows = SWAP ? W : 128;                          // token rows per unit
   static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;
   static constexpr int kBBytes = W * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStageBytes = WT ? kABytes : kABytes + kBBytes;     // WT: the token tiles have a ring of their own
   static constexpr int kStages = WT ? 2 : kSmemBudget / kStageBytes;       // operand stages
+  static constexpr int kTokStages = WT ? (ACT == 1 ? 6 : 10) : 0;          // WT: token-tile stages
   static constexpr int k8Bytes = WT ? (ACT == 1 ? 2 : 1) * 128 * kBK : 0;  // 8-bit weights of a K block
-  static constexpr int k8Stages = WT ? (kSmemBudget - kStages * kStageBytes) / k8Bytes : 0;
-  static constexpr int kRingBytes = kStages * kStageBytes + k8Stages * k8Bytes;
+  static constexpr int k8Stages =
+      WT ? (kSmemBudget - kStages * kStageBytes - kTokStages * kBBytes) / k8Bytes : 0;
+  static constexpr int kRingBytes = kStages * kStageBytes + kTokStages * kBBytes + k8Stages * k8Bytes;
   static constexpr int kOutCols = SWAP ? 128 : (ACT == 1 ? W / 2 : W);           // output columns per unit
   static constexpr int kAccCols = SWAP ? (ACT == 1 ? 2 : 1) * W : W;             // TMEM columns per unit
   static constexpr int kNumAcc = 2 * kAccCols <= 512 ? 2 : 1;
@@ -94,16 +97,17 @@ struct Cfg {
   // after the rings: the mbarriers (full/empty per stage, 2 tfull, 2 tempty,
   // done; with WT full/empty per 8-bit stage and a token barrier per operand
   // stage), the TMEM slot, the abort flag, the unit total and 8 split words
-  static constexpr int kCtrlUsed = (2 * kStages + 5 + 2 * k8Stages + (WT ? kStages : 0)) * 8 + 4 + 4 + 4 + 8 * 4;
+  static constexpr int kCtrlUsed = (2 * kStages + 5 + 2 * k8Stages + 2 * kTokStages) * 8 + 4 + 4 + 4 + 8 * 4;
   static constexpr int kCtrlBytes = (kCtrlUsed + 127) / 128 * 128;
-  // the carve, from the 1024-aligned base: operand ring | 8-bit ring | control | group arrays
-  static constexpr int kOffW8 = kStages * kStageBytes;
+  // the carve, from the 1024-aligned base: operand ring | token ring | 8-bit ring | control | group arrays
+  static constexpr int kOffTok = kStages * kStageBytes;
+  static constexpr int kOffW8 = kOffTok + kTokStages * kBBytes;
   static constexpr int kOffCtrl = kRingBytes;
   static constexpr int kOffArrays = kRingBytes + kCtrlBytes;
   static constexpr int kArrayBytes = 2 * (kMaxGroups + 1) * 4 + 128 * 4;
   static constexpr int kSmemBytes = 1024 + kOffArrays + kArrayBytes;
   static_assert(kStages >= 2, "ring too shallow");
-  static_assert(!WT || (SWAP && !MC && k8Stages >= 4), "8-bit weights: weights-on-M, a deep 8-bit ring");
+  static_assert(!WT || (SWAP && !MC && k8Stages >= kTokStages), "8-bit weights: weights-on-M, a deep 8-bit ring");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -219,6 +223,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
+  uint8_t* tok_base = smem + C::kOffTok;             // token-tile ring (WT)
   uint8_t* w8_base = smem + C::kOffW8;               // 8-bit weight ring (WT)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffCtrl);
   uint64_t* full_bar = bars;                        // [kStages]
@@ -228,8 +233,9 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   uint64_t* done_bar = tempty_bar + 2;              // [1]
   uint64_t* w8full_bar = done_bar + 1;              // [k8Stages]: 8-bit tile landed
   uint64_t* w8empty_bar = w8full_bar + C::k8Stages; // [k8Stages]: converted
-  uint64_t* tok_bar = w8empty_bar + C::k8Stages;    // [kStages]: token tile of an operand stage landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tok_bar + (WT ? C::kStages : 0));
+  uint64_t* tokfull_bar = w8empty_bar + C::k8Stages;   // [kTokStages]: token tile landed
+  uint64_t* tokempty_bar = tokfull_bar + C::kTokStages; // [kTokStages]: its MMAs are done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tokempty_bar + C::kTokStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] mode, [1] last arriver, [2..5] warp ok, [6] P, [7] S
@@ -247,11 +253,14 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   if (warp == 1 && lane == 0) {
     // with pairs a stage is free once both CTAs' MMAs are done with it (the
     // peer's multicast writes into this CTA's copy too)
-    // (WT: an operand stage is full once the four converter warps have written it)
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&full_bar[s], WT ? 4 : 1); mbar_init(&empty_bar[s], MC ? 2 : 1); }
+    // (WT: an operand stage is full once every converter warp has written it)
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full_bar[s], WT ? kConvWarps : 1);
+      mbar_init(&empty_bar[s], MC ? 2 : 1);
+    }
     if (WT) {
-      for (int s = 0; s < C::k8Stages; ++s) { mbar_init(&w8full_bar[s], 1); mbar_init(&w8empty_bar[s], 4); }
-      for (int s = 0; s < C::kStages; ++s) mbar_init(&tok_bar[s], 1);
+      for (int s = 0; s < C::k8Stages; ++s) { mbar_init(&w8full_bar[s], 1); mbar_init(&w8empty_bar[s], kConvWarps); }
+      for (int s = 0; s < C::kTokStages; ++s) { mbar_init(&tokfull_bar[s], 1); mbar_init(&tokempty_bar[s], 1); }
     }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
     mbar_init(done_bar, 1);
@@ -390,36 +399,65 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   const int wrows = ACT == 1 ? 2 * args.N : args.N;   // weight rows per group
 
   if (warp == 0 && WT) {
-    // ------------------------------------------------------------ 8-bit weight producer
+    // ------------------------------------------------------------ 8-bit weight and token producer
     // lane 0 streams the e4m3 weight tiles (gate and up, or the plain rows;
-    // 128 rows x 64 codes each) into the 8-bit ring, as deep as it goes; the
-    // converter warps take them from there
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
-      long long issued = 0;
-      int stage = 0;
-      uint32_t phase = 0;
+    // 128 rows x 64 codes each) into the 8-bit ring and the token tile of the
+    // same K block into the token ring, as far ahead as the rings go; with
+    // gathered rows the whole warp first stages the unit's source rows
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_tok = l2_policy_evict_last();
+    long long issued = 0;
+    int s8 = 0, st = 0;
+    uint32_t ph8 = 0, pht = 0;
+    WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
+    Piece pc;
+    while (wi.next(pc)) {
+      int g, row0, nrows, wb, kind;
+      decode(pc.u, g, row0, nrows, wb, kind);
+      const int wrow = g * wrows + wb * C::kOutCols;
+      const int n16 = (nrows + 15) >> 4;
+      const int nfetch = n16 * 16;
+      if (args.a_rows) {
+        __syncwarp();
+        for (int i = lane; i < nfetch; i += 32) s_gidx[i] = args.a_rows[row0 + min(i, nrows - 1)];
+        __syncwarp();
+      }
       bool ok = true;
-      WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
-      Piece pc;
-      while (ok && wi.next(pc)) {
-        int g, row0, nrows, wb, kind;
-        decode(pc.u, g, row0, nrows, wb, kind);
-        const int wrow = g * wrows + wb * C::kOutCols;
+      if (lane == 0) {
         for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
-          if (!mbar_wait(&w8empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
-          uint8_t* dst = w8_base + stage * C::k8Bytes;
-          mbar_arrive_expect_tx(&w8full_bar[stage], C::k8Bytes);
-          tma_load_2d(dst, &tm_wgt, &w8full_bar[stage], kb * kBK, wrow, pol_w);
-          if (ACT == 1) tma_load_2d(dst + 128 * kBK, &tm_wgt, &w8full_bar[stage], kb * kBK, wrow + args.N, pol_w);
+          const int kc = kb * kBK;
+          if (!mbar_wait(&w8empty_bar[s8], ph8 ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&tokempty_bar[st], pht ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+          uint8_t* dst = w8_base + s8 * C::k8Bytes;
+          mbar_arrive_expect_tx(&w8full_bar[s8], C::k8Bytes);
+          tma_load_2d(dst, &tm_wgt, &w8full_bar[s8], kc, wrow, pol_w);
+          if (ACT == 1) tma_load_2d(dst + 128 * kBK, &tm_wgt, &w8full_bar[s8], kc, wrow + args.N, pol_w);
+          uint8_t* stok = tok_base + st * C::kBBytes;
+          mbar_arrive_expect_tx(&tokfull_bar[st], static_cast<uint32_t>(nfetch * kBK * 2));
+          if (args.a_rows) {
+            for (int j = 0; j < nfetch; j += 4)
+              tma_gather4(stok + j * kBK * 2, &tm_tok, &tokfull_bar[st], kc, s_gidx[j], s_gidx[j + 1], s_gidx[j + 2],
+                          s_gidx[j + 3], pol_tok);
+          } else {
+            for (int j = 0; j < n16; ++j)
+              tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &tokfull_bar[st], kc, row0 + 16 * j, pol_tok);
+          }
           ++issued;
-          if (++stage == C::k8Stages) { stage = 0; phase ^= 1u; }
+          if (++s8 == C::k8Stages) { s8 = 0; ph8 ^= 1u; }
+          if (++st == C::kTokStages) { st = 0; pht ^= 1u; }
         }
       }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    }
+    if (lane == 0) {
       // drain: every tile issued has landed before the CTA may exit
       for (int s = 0; s < C::k8Stages; ++s) {
         const long long fills = issued / C::k8Stages + (s < issued % C::k8Stages ? 1 : 0);
         if (fills > 0) mbar_wait_timed(&w8full_bar[s], static_cast<uint32_t>((fills - 1) & 1), args.status);
+      }
+      for (int s = 0; s < C::kTokStages; ++s) {
+        const long long fills = issued / C::kTokStages + (s < issued % C::kTokStages ? 1 : 0);
+        if (fills > 0) mbar_wait_timed(&tokfull_bar[s], static_cast<uint32_t>((fills - 1) & 1), args.status);
       }
     }
   } else if (warp == 0) {
@@ -518,8 +556,8 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, tstage = 0;
+      uint32_t phase = 0, tphase = 0;
       int it = 0;
       WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
       Piece pc;
@@ -545,10 +583,13 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         bool ok = true;
         for (int kb = kb0; kb < pc.kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
-          if (WT && !mbar_wait(&tok_bar[stage], phase, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+          if (WT && !mbar_wait(&tokfull_bar[tstage], tphase, abort_flag, args.status, args.wait_ns)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * C::kStageBytes);
-          const uint32_t sb = sa + C::kABytes;
+          const uint32_t sb = WT ? smem_u32(tok_base + tstage * C::kBBytes) : sa + C::kABytes;
           const uint64_t da = smem_desc_k128(sa);
           const uint64_t db = smem_desc_k128(sb);
 #pragma unroll
@@ -573,6 +614,10 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
           else
             umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+          if (WT) {
+            umma_commit(&tokempty_bar[tstage]);
+            if (++tstage == C::kTokStages) { tstage = 0; tphase ^= 1u; }
+          }
         }
         if (!ok) break;
         umma_commit(&tfull_bar[ab]);           // accumulator ab ready for the epilogue
@@ -792,59 +837,32 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     }
   } else if constexpr (WT) {
     // ------------------------------------------------------------ converters
-    // warps 6..9: an 8-bit weight stage -> the bf16 operand tile(s) of an
+    // warps 6..: an 8-bit weight stage -> the bf16 operand tile(s) of an
     // operand stage, in the 128-byte swizzle the MMA reads (the 16-byte chunk
-    // c of row r lands at chunk c ^ (r & 7) of the row); converter warp 0 also
-    // loads the stage's token tile.  A stage is full when all four warps have
-    // written it (their writes fenced for the async proxy) and its token tile
-    // has landed.
-    const int cw = warp - 6;
+    // c of row r lands at chunk c ^ (r & 7) of the row).  A stage is full when
+    // every converter warp has written its share (the writes fenced for the
+    // async proxy).
     const int ct = threadIdx.x - 192;
-    const uint64_t pol_tok = l2_policy_evict_last();
     int stage = 0, s8 = 0;
     uint32_t phase = 0, ph8 = 0;
-    long long tok_issued = 0;
     bool ok = true;
     WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
     Piece pc;
     while (ok && wi.next(pc)) {
-      int g, row0, nrows, wb, kind;
-      decode(pc.u, g, row0, nrows, wb, kind);
-      const int n16 = (nrows + 15) >> 4;
-      const int nfetch = n16 * 16;
-      if (args.a_rows && cw == 0) {
-        __syncwarp();
-        for (int i = lane; i < nfetch; i += 32) s_gidx[i] = args.a_rows[row0 + min(i, nrows - 1)];
-        __syncwarp();
-      }
       for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
         ok = __all_sync(0xffffffffu, mbar_wait(&w8full_bar[s8], ph8, abort_flag, args.status, args.wait_ns));
         if (ok)
           ok = __all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns));
         if (!ok) break;
         uint8_t* sa = stage_base + stage * C::kStageBytes;
-        if (cw == 0 && lane == 0) {
-          const int kc = kb * kBK;
-          uint8_t* stok = sa + C::kABytes;
-          mbar_arrive_expect_tx(&tok_bar[stage], static_cast<uint32_t>(nfetch * kBK * 2));
-          if (args.a_rows) {
-            for (int j = 0; j < nfetch; j += 4)
-              tma_gather4(stok + j * kBK * 2, &tm_tok, &tok_bar[stage], kc, s_gidx[j], s_gidx[j + 1], s_gidx[j + 2],
-                          s_gidx[j + 3], pol_tok);
-          } else {
-            for (int j = 0; j < n16; ++j)
-              tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &tok_bar[stage], kc, row0 + 16 * j, pol_tok);
-          }
-          ++tok_issued;
-        }
         const uint8_t* src = w8_base + s8 * C::k8Bytes;
         constexpr int kChunks = C::k8Bytes / 8;   // 8 codes each: tile, row, 16-byte chunk of the bf16 row
 #pragma unroll 4
-        for (int i = ct; i < kChunks; i += 128) {
+        for (int i = ct; i < kChunks; i += 32 * kConvWarps) {
           const int tile = i >> 10, r = (i >> 3) & 127, c = i & 7;
           const uint2 v = *reinterpret_cast<const uint2*>(src + i * 8);
-          const uint4 o = make_uint4(e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y),
-                                     e4m3x2_to_bf16x2(v.y >> 16));
+          const uint2 lo = e4m3x4_to_bf16x4(v.x), hi = e4m3x4_to_bf16x4(v.y);
+          const uint4 o = make_uint4(lo.x, lo.y, hi.x, hi.y);
           *reinterpret_cast<uint4*>(sa + tile * kTileRows128 + r * 128 + ((c ^ (r & 7)) << 4)) = o;
         }
         fence_proxy_async_smem();
@@ -855,13 +873,6 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         }
         if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         if (++s8 == C::k8Stages) { s8 = 0; ph8 ^= 1u; }
-      }
-    }
-    if (cw == 0 && lane == 0) {
-      // drain: every token tile issued has landed before the CTA may exit
-      for (int s = 0; s < C::kStages; ++s) {
-        const long long fills = tok_issued / C::kStages + (s < tok_issued % C::kStages ? 1 : 0);
-        if (fills > 0) mbar_wait_timed(&tok_bar[s], static_cast<uint32_t>((fills - 1) & 1), args.status);
       }
     }
   }

@@ -65,6 +65,11 @@ WORKLOADS = {
     # large prefill: Zipf(1.2) bias, 8 forced-empty experts, one hot expert
     "large_prefill": Workload("large_prefill", 16384, 4096, 256, 8, 1024, 4096,
                               sigma_router=0.02, zipf_s=1.2, n_empty=8),
+    # the decode shapes with FP8 (e4m3, per-row scales) routed expert weights
+    # (make_inputs_w8 / make_expert_weights_w8 draw them)
+    "decode_w8": Workload("decode_w8", 8, 2048, 128, 8, 768, 2048, sigma_router=0.02),
+    "batched_decode_w8": Workload("batched_decode_w8", 256, 2048, 128, 8, 768, 2048,
+                                  sigma_router=0.02, zipf_s=1.1),
 }
 
 # every (workload, T) the parity tests cover at full size

@@ -90,6 +90,30 @@ def test_grouped_gemm_w8(rows, N, K, act, use_ws):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
+def test_grouped_gemm_w8_every_code_exact():
+    """Every e4m3 code at every position of the tiles: token rows that are unit
+    vectors pick single weights, so with power-of-two scales each output is one
+    decoded code times its scale, exact in bf16, and must match bit for bit
+    (codes 0x01..0x07 and 0x81..0x87 are the subnormals m * 2^-9)."""
+    G, per, N, K = 4, 64, 128, 256
+    off = (np.arange(G + 1) * per).astype(np.int32)
+    R = G * per
+    a = np.zeros((R, K), dtype=np.float32)
+    a[np.arange(R), np.arange(R) % K] = 1.0
+    a_bits = synth.f32_to_bf16_bits(a)
+    n, k = np.meshgrid(np.arange(N), np.arange(K), indexing="ij")
+    codes = np.stack([(n * 3 + k + 17 * g) % 256 for g in range(G)]).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x00
+    scale = np.ldexp(1.0, (np.arange(G * N) % 7) - 3).reshape(G, N).astype(np.float32)
+    ref = om.grouped_gemm(a_bits, codes, off, 0, w_scale=scale)
+    out = torch.empty((R, N), dtype=torch.bfloat16, device="cuda")
+    B.moe_grouped_gemm_w8(bf16_tensor(a_bits, "cuda"), u8(codes), f32(scale), i32(off), G, R, N, K, 0, out, None, 0,
+                          stream())
+    no_device_error()
+    assert np.array_equal(to_f64(out), ref)
+    assert len(np.unique(codes)) == 254
+
+
 @pytest.mark.parametrize("act,N,K", [(1, 768, 2048), (0, 2048, 768), (1, 256, 512)])
 def test_grouped_gemm_w8_one_row_groups(act, N, K):
     """Groups of one row (a token's k experts): the CUDA-core weight stream
