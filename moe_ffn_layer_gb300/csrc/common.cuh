@@ -159,6 +159,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// mbar_wait for roles that wait long and are not on the critical path (an
+// epilogue waiting for its accumulator): between tests the warp sleeps about
+// `sleep_ns`, leaving the issue slots to the warps that work meanwhile.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                                uint64_t limit_ns, uint32_t sleep_ns) {
+  if (limit_ns == 0) return mbar_wait(bar, parity, abort, status, 0);
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      set_status(status, MOE_ERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Wait bounded by time only (used when draining copies in flight).
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity, int* status) {
   const uint64_t t0 = globaltimer();
@@ -169,6 +189,24 @@ __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity, 
       return false;
     }
   }
+}
+
+// Shared-memory loads and stores by 32-bit shared address (the address
+// space stated, whatever the compiler can prove about a pointer).
+__device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_u4(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
@@ -260,6 +298,19 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T: A (M rows x 16 bf16) in tensor
+// memory, row m in lane m, K elements 2c and 2c+1 in column c (the even one
+// in the low half); the next 16-element K step is 8 columns on.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -311,6 +362,27 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
+// 16 / 32 registers per thread -> 32 lanes x that many consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile stored with the
@@ -363,20 +435,25 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
 // code's sign put at bit 15 of a 16-bit half and its exponent and mantissa at
 // bits 10..4 read as the bf16 2^(e-127) * 1.m, or the subnormal 0.m * 2^-126
 // for e = 0; one bf16 multiply by 2^120 moves the bias from 127 to 7, exactly
-// (every e4m3 value is a normal bf16).  The byte permute puts codes 0 and 1 in
-// the high bytes of the two halves, and codes 2 and 3 after a shift by 8.
+// (every e4m3 value is a normal bf16).  The byte permute builds, per half, the
+// code in the low byte over a byte of copies of its sign bit (prmt's
+// sign-replicate selector); shifted left by 4, the mask keeps the sign copy at
+// bit 15 and the exponent and mantissa at bits 10..4.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t v) {
-  constexpr uint32_t kTwo120 = 0x7B807B80u;  // 2^120 in both halves
-  const uint32_t q = __byte_perm(v, 0u, 0x1302);  // bytes: code 2, code 0, code 3, code 1
-  const uint32_t r = q << 8;                      // codes 2 and 3 in the high bytes
-  const uint32_t x = (q & 0x80008000u) | ((q >> 4) & 0x07F007F0u);
-  const uint32_t y = (r & 0x80008000u) | ((r >> 4) & 0x07F007F0u);
-  return make_uint2(bf16x2_mul(x, kTwo120), bf16x2_mul(y, kTwo120));
+  constexpr uint32_t kTwo120 = 0x7B807B80u;                 // 2^120 in both halves
+  const uint32_t u = prmt(v, 0u, 0x9180u) << 4;           // code 0, sign(0), code 1, sign(1)
+  const uint32_t w = prmt(v, 0u, 0xB3A2u) << 4;           // code 2, sign(2), code 3, sign(3)
+  return make_uint2(bf16x2_mul(u & 0x87F087F0u, kTwo120), bf16x2_mul(w & 0x87F087F0u, kTwo120));
 }
 
 // Eight e4m3 codes (v.x bytes 0..3, then v.y) as floats.

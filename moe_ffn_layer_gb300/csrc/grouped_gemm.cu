@@ -32,6 +32,14 @@
 // Roles:  warp 0      TMA producer into a STAGES-deep shared-memory ring
 //         warp 1      tensor-memory allocator and MMA issuer (one thread)
 //         warps 2..5  epilogue: tcgen05.ld -> SiLU*mul or identity -> bf16
+// With e4m3 weights (weights-on-M only) warp 0 streams the 8-bit tiles into
+// their own ring, warps 6..13 widen them to bf16 in tensor memory (the MMA's A
+// operand), warp 14 loads the token tiles into a ring of their own, and the
+// epilogue multiplies each row by its scale.  Measured on GB300: one thread
+// issues a 128 x 16 x 16 MMA at best every ~50 cycles (two issuing threads
+// reach the tensor pipe's ~39), and with its barrier waits and commits the
+// issuer needs ~1,400 cycles per 64-wide K step of a gate/up tile pair; so at
+// decode sizes the 8-bit stream runs at the MMA issue rate, not at HBM speed.
 // The unit list is built on the device from the group offsets (no host sync):
 // group g contributes ceil(rows_g / R) x NB units, R = rows per unit, NB =
 // weight blocks; empty groups contribute none.  Units are ordered (group,
@@ -71,21 +79,25 @@ constexpr int tmem_cols_pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 
 // loads its own weights and 64 of the tile's token rows).
 //
 // WT = 1 (weights-on-M only): the weights are e4m3 codes with one fp32 scale
-// per weight row.  The producer streams the 8-bit weight tiles and the token
-// tiles into their own rings (the bytes in flight from HBM); eight converter
-// warps turn each 8-bit tile into the bf16 operand tile of a two-stage
-// operand ring (exact: every e4m3 value is a bf16 value); the epilogue
-// multiplies each accumulator row by its scale.
+// per weight row.  The producer streams the 8-bit weight tiles into a deep
+// ring of their own (the bytes in flight from HBM), limited by nothing but
+// that ring; a token producer warp fills a short token ring (tokens come from
+// L2); eight converter warps widen each 8-bit tile to bf16 (exact: every e4m3
+// value is a bf16 value) straight into tensor memory, where the MMA reads its
+// A operand (a ring of kStages A stages beside the accumulators), so shared
+// memory holds only the 8-bit and token rings; the epilogue multiplies each
+// accumulator row by its scale.
 constexpr int kConvWarps = 8;
 template <int SWAP, int W, int ACT, int MC = 0, int WT = 0>
 struct Cfg {
-  static constexpr int kThreads = WT ? 192 + 32 * kConvWarps : 192;   // 6 warps (+ the converter warps)
+  // 6 warps (+ the converter warps and the token producer warp)
+  static constexpr int kThreads = WT ? 192 + 32 * (kConvWarps + 1) : 192;
   static constexpr int kUnitRows = SWAP ? W : 128;                          // token rows per unit
   static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;
   static constexpr int kBBytes = W * kBK * 2;
-  static constexpr int kStageBytes = WT ? kABytes : kABytes + kBBytes;     // WT: the token tiles have a ring of their own
-  static constexpr int kStages = WT ? 2 : kSmemBudget / kStageBytes;       // operand stages
-  static constexpr int kTokStages = WT ? (ACT == 1 ? 6 : 10) : 0;          // WT: token-tile stages
+  static constexpr int kStageBytes = WT ? 0 : kABytes + kBBytes;           // WT: A in tensor memory, tokens apart
+  static constexpr int kStages = WT ? 4 : kSmemBudget / kStageBytes;       // operand stages
+  static constexpr int kTokStages = WT ? 4 : 0;                            // WT: token-tile stages
   static constexpr int k8Bytes = WT ? (ACT == 1 ? 2 : 1) * 128 * kBK : 0;  // 8-bit weights of a K block
   static constexpr int k8Stages =
       WT ? (kSmemBudget - kStages * kStageBytes - kTokStages * kBBytes) / k8Bytes : 0;
@@ -93,7 +105,10 @@ struct Cfg {
   static constexpr int kOutCols = SWAP ? 128 : (ACT == 1 ? W / 2 : W);           // output columns per unit
   static constexpr int kAccCols = SWAP ? (ACT == 1 ? 2 : 1) * W : W;             // TMEM columns per unit
   static constexpr int kNumAcc = 2 * kAccCols <= 512 ? 2 : 1;
-  static constexpr int kTmemCols = tmem_cols_pow2(kNumAcc * kAccCols);
+  // WT: tensor-memory columns of one A stage (128 rows x 64 bf16 per tile), after the accumulators
+  static constexpr int kACols = WT ? (ACT == 1 ? 2 : 1) * kBK / 2 : 0;
+  static constexpr int kAColBase = kNumAcc * kAccCols;
+  static constexpr int kTmemCols = tmem_cols_pow2(kAColBase + kStages * kACols);
   // after the rings: the mbarriers (full/empty per stage, 2 tfull, 2 tempty,
   // done; with WT full/empty per 8-bit stage and a token barrier per operand
   // stage), the TMEM slot, the abort flag, the unit total and 8 split words
@@ -108,6 +123,7 @@ struct Cfg {
   static constexpr int kSmemBytes = 1024 + kOffArrays + kArrayBytes;
   static_assert(kStages >= 2, "ring too shallow");
   static_assert(!WT || (SWAP && !MC && k8Stages >= kTokStages), "8-bit weights: weights-on-M, a deep 8-bit ring");
+  static_assert(!WT || kAColBase + kStages * kACols <= 512, "8-bit weights: A stages beside the accumulators");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -399,65 +415,36 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   const int wrows = ACT == 1 ? 2 * args.N : args.N;   // weight rows per group
 
   if (warp == 0 && WT) {
-    // ------------------------------------------------------------ 8-bit weight and token producer
+    // ------------------------------------------------------------ 8-bit weight producer
     // lane 0 streams the e4m3 weight tiles (gate and up, or the plain rows;
-    // 128 rows x 64 codes each) into the 8-bit ring and the token tile of the
-    // same K block into the token ring, as far ahead as the rings go; with
-    // gathered rows the whole warp first stages the unit's source rows
+    // 128 rows x 64 codes each) into the 8-bit ring, as far ahead as it goes
     const uint64_t pol_w = l2_policy_evict_first();
-    const uint64_t pol_tok = l2_policy_evict_last();
     long long issued = 0;
-    int s8 = 0, st = 0;
-    uint32_t ph8 = 0, pht = 0;
-    WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
-    Piece pc;
-    while (wi.next(pc)) {
-      int g, row0, nrows, wb, kind;
-      decode(pc.u, g, row0, nrows, wb, kind);
-      const int wrow = g * wrows + wb * C::kOutCols;
-      const int n16 = (nrows + 15) >> 4;
-      const int nfetch = n16 * 16;
-      if (args.a_rows) {
-        __syncwarp();
-        for (int i = lane; i < nfetch; i += 32) s_gidx[i] = args.a_rows[row0 + min(i, nrows - 1)];
-        __syncwarp();
-      }
+    int s8 = 0;
+    uint32_t ph8 = 0;
+    if (lane == 0) {
+      WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
+      Piece pc;
       bool ok = true;
-      if (lane == 0) {
+      while (ok && wi.next(pc)) {
+        int g, row0, nrows, wb, kind;
+        decode(pc.u, g, row0, nrows, wb, kind);
+        const int wrow = g * wrows + wb * C::kOutCols;
         for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
-          const int kc = kb * kBK;
           if (!mbar_wait(&w8empty_bar[s8], ph8 ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
-          if (!mbar_wait(&tokempty_bar[st], pht ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
           uint8_t* dst = w8_base + s8 * C::k8Bytes;
           mbar_arrive_expect_tx(&w8full_bar[s8], C::k8Bytes);
-          tma_load_2d(dst, &tm_wgt, &w8full_bar[s8], kc, wrow, pol_w);
-          if (ACT == 1) tma_load_2d(dst + 128 * kBK, &tm_wgt, &w8full_bar[s8], kc, wrow + args.N, pol_w);
-          uint8_t* stok = tok_base + st * C::kBBytes;
-          mbar_arrive_expect_tx(&tokfull_bar[st], static_cast<uint32_t>(nfetch * kBK * 2));
-          if (args.a_rows) {
-            for (int j = 0; j < nfetch; j += 4)
-              tma_gather4(stok + j * kBK * 2, &tm_tok, &tokfull_bar[st], kc, s_gidx[j], s_gidx[j + 1], s_gidx[j + 2],
-                          s_gidx[j + 3], pol_tok);
-          } else {
-            for (int j = 0; j < n16; ++j)
-              tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &tokfull_bar[st], kc, row0 + 16 * j, pol_tok);
-          }
+          tma_load_2d(dst, &tm_wgt, &w8full_bar[s8], kb * kBK, wrow, pol_w);
+          if (ACT == 1) tma_load_2d(dst + 128 * kBK, &tm_wgt, &w8full_bar[s8], kb * kBK, wrow + args.N, pol_w);
           ++issued;
           if (++s8 == C::k8Stages) { s8 = 0; ph8 ^= 1u; }
-          if (++st == C::kTokStages) { st = 0; pht ^= 1u; }
         }
       }
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-    }
-    if (lane == 0) {
       // drain: every tile issued has landed before the CTA may exit
+      constexpr int n8 = C::k8Stages > 0 ? C::k8Stages : 1;
       for (int s = 0; s < C::k8Stages; ++s) {
-        const long long fills = issued / C::k8Stages + (s < issued % C::k8Stages ? 1 : 0);
+        const long long fills = issued / n8 + (s < issued % n8 ? 1 : 0);
         if (fills > 0) mbar_wait_timed(&w8full_bar[s], static_cast<uint32_t>((fills - 1) & 1), args.status);
-      }
-      for (int s = 0; s < C::kTokStages; ++s) {
-        const long long fills = issued / C::kTokStages + (s < issued % C::kTokStages ? 1 : 0);
-        if (fills > 0) mbar_wait_timed(&tokfull_bar[s], static_cast<uint32_t>((fills - 1) & 1), args.status);
       }
     }
   } else if (warp == 0) {
@@ -596,7 +583,14 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // +32 bytes per 16-element K step inside the 128-byte swizzle row
             const uint64_t ka = static_cast<uint64_t>(kk * 2);
-            if (SWAP) {
+            if (WT) {
+              // A from tensor memory: 8 columns per 16-element K step; the up tile 32 columns on
+              const int c = kk & (chains - 1);
+              const uint32_t acc = (kb > kb0 || kk >= chains) ? 1u : 0u;
+              const uint32_t ta = tmem_base + C::kAColBase + stage * C::kACols + kk * 8;
+              umma_bf16_ts(d_tmem + c * cw, ta, db + ka, idesc, acc);
+              if (ACT == 1) umma_bf16_ts(d_tmem + (chains + c) * cw, ta + kBK / 2, db + ka, idesc, acc);
+            } else if (SWAP) {
               const int c = kk & (chains - 1);
               const uint32_t acc = (kb > kb0 || kk >= chains) ? 1u : 0u;
               umma_bf16(d_tmem + c * cw, da + ka, db + ka, idesc, acc);
@@ -640,7 +634,10 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
       int g, row0, nrows, wb, kind;
       decode(u, g, row0, nrows, wb, kind);
       // the warp leaves together or not at all (tcgen05.ld below is warp-wide)
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[ab], aphase, abort_flag, args.status, args.wait_ns));
+      // (8-bit weights: the converter warps need the issue slots while this waits)
+      bool ok = __all_sync(0xffffffffu, WT ? mbar_wait_sleep(&tfull_bar[ab], aphase, abort_flag, args.status,
+                                                             args.wait_ns, 256)
+                                           : mbar_wait(&tfull_bar[ab], aphase, abort_flag, args.status, args.wait_ns));
       if (P > 1) {
         // the split path meets at named barriers: the four warps leave together or not at all
         if (lane == 0) s_split[2 + q] = ok ? 1 : 0;
@@ -835,14 +832,72 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         release_acc();
       }
     }
+  } else if (WT && warp == 6 + kConvWarps) {
+    // ------------------------------------------------------------ token producer
+    // lane 0 loads the token tile of each K block (the unit's rows: 16-row
+    // tiles, or gathered rows) into the token ring; with gathered rows the
+    // whole warp first stages the unit's source rows
+    const uint64_t pol_tok = l2_policy_evict_last();
+    long long issued = 0;
+    int st = 0;
+    uint32_t pht = 0;
+    WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
+    Piece pc;
+    while (wi.next(pc)) {
+      int g, row0, nrows, wb, kind;
+      decode(pc.u, g, row0, nrows, wb, kind);
+      const int n16 = (nrows + 15) >> 4;
+      const int nfetch = n16 * 16;
+      if (args.a_rows) {
+        __syncwarp();
+        for (int i = lane; i < nfetch; i += 32) s_gidx[i] = args.a_rows[row0 + min(i, nrows - 1)];
+        __syncwarp();
+      }
+      bool ok = true;
+      if (lane == 0) {
+        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
+          const int kc = kb * kBK;
+          if (!mbar_wait(&tokempty_bar[st], pht ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+          uint8_t* stok = tok_base + st * C::kBBytes;
+          mbar_arrive_expect_tx(&tokfull_bar[st], static_cast<uint32_t>(nfetch * kBK * 2));
+          if (args.a_rows) {
+            for (int j = 0; j < nfetch; j += 4)
+              tma_gather4(stok + j * kBK * 2, &tm_tok, &tokfull_bar[st], kc, s_gidx[j], s_gidx[j + 1], s_gidx[j + 2],
+                          s_gidx[j + 3], pol_tok);
+          } else {
+            for (int j = 0; j < n16; ++j)
+              tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &tokfull_bar[st], kc, row0 + 16 * j, pol_tok);
+          }
+          ++issued;
+          if (++st == C::kTokStages) { st = 0; pht ^= 1u; }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    }
+    if (lane == 0) {
+      // drain: every tile issued has landed before the CTA may exit
+      constexpr int nt = C::kTokStages > 0 ? C::kTokStages : 1;
+      for (int s = 0; s < C::kTokStages; ++s) {
+        const long long fills = issued / nt + (s < issued % nt ? 1 : 0);
+        if (fills > 0) mbar_wait_timed(&tokfull_bar[s], static_cast<uint32_t>((fills - 1) & 1), args.status);
+      }
+    }
   } else if constexpr (WT) {
     // ------------------------------------------------------------ converters
-    // warps 6..: an 8-bit weight stage -> the bf16 operand tile(s) of an
-    // operand stage, in the 128-byte swizzle the MMA reads (the 16-byte chunk
-    // c of row r lands at chunk c ^ (r & 7) of the row).  A stage is full when
-    // every converter warp has written its share (the writes fenced for the
-    // async proxy).
-    const int ct = threadIdx.x - 192;
+    // warps 6..13: an 8-bit weight stage -> bf16 A stage in tensor memory.  A
+    // warp may touch only its lane quadrant (warp mod 4), so each thread owns
+    // one weight row r of the tile: with gate and up tiles the quadrant's first
+    // warp widens the gate row and its second the up row (64 codes -> 32
+    // columns each); a plain tile is split in K halves (32 codes -> 16
+    // columns).  The 8-bit tile comes in the 64-byte swizzle, in which the
+    // 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3), so that the
+    // row-per-lane reads meet no bank conflicts.  A stage is full when every
+    // converter warp's stores have completed.
+    const int quad = warp & 3;
+    const int half = (warp - 6) >> 2;
+    const int r = quad * 32 + lane;
+    const uint32_t rsw = static_cast<uint32_t>((r >> 1) & 3);
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase;
     int stage = 0, s8 = 0;
     uint32_t phase = 0, ph8 = 0;
     bool ok = true;
@@ -854,18 +909,38 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         if (ok)
           ok = __all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns));
         if (!ok) break;
-        uint8_t* sa = stage_base + stage * C::kStageBytes;
-        const uint8_t* src = w8_base + s8 * C::k8Bytes;
-        constexpr int kChunks = C::k8Bytes / 8;   // 8 codes each: tile, row, 16-byte chunk of the bf16 row
-#pragma unroll 4
-        for (int i = ct; i < kChunks; i += 32 * kConvWarps) {
-          const int tile = i >> 10, r = (i >> 3) & 127, c = i & 7;
-          const uint2 v = *reinterpret_cast<const uint2*>(src + i * 8);
-          const uint2 lo = e4m3x4_to_bf16x4(v.x), hi = e4m3x4_to_bf16x4(v.y);
-          const uint4 o = make_uint4(lo.x, lo.y, hi.x, hi.y);
-          *reinterpret_cast<uint4*>(sa + tile * kTileRows128 + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+        tc_fence_after();
+        const uint32_t src = smem_u32(w8_base + s8 * C::k8Bytes) + (ACT == 1 ? half * 128 * kBK : 0) + r * kBK;
+        const uint32_t dst = t_row + stage * C::kACols;
+        if (ACT == 1) {
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = lds_u4(src + ((static_cast<uint32_t>(j) ^ rsw) << 4));
+          uint32_t o[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint2 a0 = e4m3x4_to_bf16x4(v[j].x), a1 = e4m3x4_to_bf16x4(v[j].y);
+            const uint2 a2 = e4m3x4_to_bf16x4(v[j].z), a3 = e4m3x4_to_bf16x4(v[j].w);
+            o[8 * j + 0] = a0.x; o[8 * j + 1] = a0.y; o[8 * j + 2] = a1.x; o[8 * j + 3] = a1.y;
+            o[8 * j + 4] = a2.x; o[8 * j + 5] = a2.y; o[8 * j + 6] = a3.x; o[8 * j + 7] = a3.y;
+          }
+          tmem_st_32cols(dst + half * (kBK / 2), o);
+        } else {
+          uint4 v[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) v[j] = lds_u4(src + ((static_cast<uint32_t>(2 * half + j) ^ rsw) << 4));
+          uint32_t o[16];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint2 a0 = e4m3x4_to_bf16x4(v[j].x), a1 = e4m3x4_to_bf16x4(v[j].y);
+            const uint2 a2 = e4m3x4_to_bf16x4(v[j].z), a3 = e4m3x4_to_bf16x4(v[j].w);
+            o[8 * j + 0] = a0.x; o[8 * j + 1] = a0.y; o[8 * j + 2] = a1.x; o[8 * j + 3] = a1.y;
+            o[8 * j + 4] = a2.x; o[8 * j + 5] = a2.y; o[8 * j + 6] = a3.x; o[8 * j + 7] = a3.y;
+          }
+          tmem_st_16cols(dst + half * (kBK / 4), o);
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&full_bar[stage]);
@@ -920,8 +995,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D byte tensor [rows][cols] (e4m3 weights), box [box_rows][64 bytes], no
-// swizzle (the converter warps read it row by row).
+// 2-D byte tensor [rows][cols] (e4m3 weights), box [box_rows][64 bytes], in
+// the 64-byte swizzle (the converter warps read it one row per lane).
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -930,7 +1005,7 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
