@@ -389,12 +389,20 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
   const int rows = T * d->k;
   int n = 0;
 
+  // One token with a shared expert: three launches and no side stream.  The
+  // router lets the gate_up weight stream start at once; that launch first
+  // computes the shared expert's gate_up (it needs only x) while the router
+  // runs, then the routed rows; the down launch computes the shared expert's
+  // down beside the routed ones and adds it in the combine.
+  const bool one_token_fused = T == 1 && has_shared && d->I_s % 8 == 0 &&
+                               moe::down_combine_gemv_applies(d->E, d->H, d->I, d->k) &&
+                               moe::grouped_gemv_applies(d->E, d->I, d->H, 1, 1);
   // SMs for the two streams.  At decode sizes both are weight streams that
   // run side by side for the whole call: the shared expert gets the SMs in
   // proportion to its share of the weight bytes (at least 8, at most half),
   // the routed matmuls the rest.  Larger batches give both streams every SM.
   int side_sms = di->sms, main_sms = di->sms;
-  if (T <= moe::route_small_max_tokens() && has_shared) {
+  if (T <= moe::route_small_max_tokens() && has_shared && !one_token_fused) {
     const double shared_bytes = 3.0 * d->I_s * d->H * 2;
     const double routed_bytes = 3.0 * d->I * d->H * 2 * std::min<long long>(d->E, static_cast<long long>(T) * d->k);
     int c = static_cast<int>(di->sms * shared_bytes / (shared_bytes + routed_bytes) + 0.5);
@@ -420,13 +428,13 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
   if (T <= moe::route_small_max_tokens()) {
     // decode sizes: the shared expert streams its weights while one router
     // launch routes and dispatches
-    rc = fork_shared();
+    if (!one_token_fused) rc = fork_shared();
     // router, top-k and counting sort in one launch
     const moe::DispatchOut dout{offsets, sorted, inv};
     if (!rc)
       rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits,
                              reinterpret_cast<unsigned int*>(base + L.route_ticket), &dout, di->status, di->sms,
-                             stream, &n);
+                             stream, &n, one_token_fused);
   } else {
     const int fork_at = fork_stage(d, T);
     if (fork_at == 0) rc = fork_shared();
@@ -444,7 +452,10 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
     // sorted_token (TMA gather4, a few rows per stage); larger batches read the
     // permuted copy, since one producer thread issuing a gather per 4 rows
     // cannot feed full 128-row tiles
-    rc = T <= moe::route_small_max_tokens()
+    rc = one_token_fused
+             ? moe::grouped_gemv_launch(x, w->w_gate_up, w->s_gate_up, offsets, d->E, rows, d->I, d->H, 1, h,
+                                        di->status, stream, &n, sorted, T, 1, di->sms, x, w->ws_gate_up, d->I_s, hs)
+         : T <= moe::route_small_max_tokens()
              ? moe::grouped_gemm_launch(x, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, &gmain,
                                         main_sms, stream, &n, sorted, T, 0, T, w->s_gate_up)
              : moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status,
@@ -457,9 +468,11 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
                                   main_sms, stream, &n, nullptr, 0, 0, T, w->s_down);
   if (rc) return rc;
   // join, then combine
-  if (has_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  if (has_shared && !one_token_fused && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
   rc = fused_tail ? moe::down_combine_gemv_launch(h, w->w_down, w->s_down, offsets, d->E, d->H, d->I, d->k, inv, tw,
-                                                  has_shared ? s : nullptr, out, di->status, stream, &n)
+                                                  has_shared && !one_token_fused ? s : nullptr, out, di->status,
+                                                  stream, &n, one_token_fused ? w->ws_down : nullptr,
+                                                  one_token_fused ? hs : nullptr, d->I_s)
                   : moe::combine_launch(y, inv, tw, has_shared ? s : nullptr, T, d->H, d->k, rows, out, stream, &n);
   t_last_launches = n;
   return rc;

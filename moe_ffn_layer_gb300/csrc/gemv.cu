@@ -117,29 +117,17 @@ __device__ __forceinline__ void list_groups(const int32_t* __restrict__ offsets,
 // product is row a_rows[r] of `a` when a_rows is given, else row r.  R >= the
 // rows of any group (1, 2 or 4).  WT 1: W holds e4m3 codes and wscale one fp32
 // scale per weight row ([G][2N] or [G][N]), applied to each dot product.
+// One warp, one item: output block n0 (one column with SiLU*mul, kRowsDown
+// without) of group g, whose token rows are r0 .. r0 + nr - 1.
 template <int ACT, int R, int WT>
-__global__ void __launch_bounds__(kGemvThreads)
-    grouped_gemv_kernel(const __nv_bfloat16* __restrict__ a, const uint8_t* __restrict__ w,
-                        const float* __restrict__ wscale, const int32_t* __restrict__ offsets, int G, int rows_max,
-                        int N, int K, const int32_t* __restrict__ a_rows, int a_src_rows,
-                        __nv_bfloat16* __restrict__ out, int* status) {
+__device__ __forceinline__ void gemv_item(const __nv_bfloat16* __restrict__ a, const uint8_t* __restrict__ w,
+                                          const float* __restrict__ wscale, int g, int n0, int r0, int nr, int N,
+                                          int K, const int32_t* __restrict__ a_rows, int a_src_rows, int rows_max,
+                                          __nv_bfloat16* __restrict__ out) {
   using WC = WeightChunk<WT>;
   constexpr int NW = ACT == 1 ? 2 : kRowsDown;   // weight rows per warp
   constexpr int NPW = ACT == 1 ? 1 : kRowsDown;  // output columns per warp
-  __shared__ int s_groups[kMaxGemvGroups];
-  __shared__ int s_count;
-  chain_wait();
-  const ChainReleaseAtExit release_next;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  list_groups(offsets, G, rows_max, R, status, s_groups, &s_count);
-  const int blocks = N / NPW;                     // output blocks per group
-  const long long items = static_cast<long long>(s_count) * blocks;
-  for (long long item = static_cast<long long>(blockIdx.x) * (kGemvThreads / 32) + warp; item < items;
-       item += static_cast<long long>(gridDim.x) * (kGemvThreads / 32)) {
-  const int g = s_groups[item / blocks];
-  const int n0 = static_cast<int>(item % blocks) * NPW;
-  const int r0 = offsets ? offsets[g] : 0;
-  const int nr = (offsets ? offsets[g + 1] : rows_max) - r0;
+  const int lane = threadIdx.x & 31;
   // this warp's weight rows and token rows (rows past nr repeat the last one)
   const size_t wrows = ACT == 1 ? 2 * static_cast<size_t>(N) : N;
   const uint8_t* wr[NW];
@@ -219,6 +207,49 @@ __global__ void __launch_bounds__(kGemvThreads)
       }
     }
   }
+}
+
+// A one-row SiLU*mul matmul (bf16 weights, one group) that a grouped_gemv
+// launch runs before it waits on the previous kernel of its stream: work that
+// does not depend on that kernel (the shared expert's gate_up at one token,
+// which needs only x).  Only a launch whose predecessor lets dependents start
+// after its own wait on its predecessor has returned may carry one (the
+// router does so at one token), so that x is complete and `out` is no longer
+// read by the call before.
+struct GemvPre {
+  const __nv_bfloat16* a;   // [1][K]
+  const uint8_t* w;         // [2N][K] bf16, gate rows first; nullptr: none
+  int N;
+  __nv_bfloat16* out;       // [1][N]
+};
+
+// (two CTAs per SM: the weight stream needs the loads of 16 warps in flight)
+template <int ACT, int R, int WT>
+__global__ void __launch_bounds__(kGemvThreads, 2)
+    grouped_gemv_kernel(const __nv_bfloat16* __restrict__ a, const uint8_t* __restrict__ w,
+                        const float* __restrict__ wscale, const int32_t* __restrict__ offsets, int G, int rows_max,
+                        int N, int K, const int32_t* __restrict__ a_rows, int a_src_rows,
+                        __nv_bfloat16* __restrict__ out, int* status, const GemvPre pre) {
+  constexpr int NPW = ACT == 1 ? 1 : kRowsDown;  // output columns per warp
+  __shared__ int s_groups[kMaxGemvGroups];
+  __shared__ int s_count;
+  const int warp = threadIdx.x >> 5;
+  const long long wstride = static_cast<long long>(gridDim.x) * (kGemvThreads / 32);
+  const long long wfirst = static_cast<long long>(blockIdx.x) * (kGemvThreads / 32) + warp;
+  if (pre.w)
+    for (long long item = wfirst; item < pre.N; item += wstride)
+      gemv_item<1, 1, 0>(pre.a, pre.w, nullptr, 0, static_cast<int>(item), 0, 1, pre.N, K, nullptr, 0, 1, pre.out);
+  chain_wait();
+  const ChainReleaseAtExit release_next;
+  list_groups(offsets, G, rows_max, R, status, s_groups, &s_count);
+  const int blocks = N / NPW;                     // output blocks per group
+  const long long items = static_cast<long long>(s_count) * blocks;
+  for (long long item = wfirst; item < items; item += wstride) {
+    const int g = s_groups[item / blocks];
+    const int n0 = static_cast<int>(item % blocks) * NPW;
+    const int r0 = offsets ? offsets[g] : 0;
+    const int nr = (offsets ? offsets[g + 1] : rows_max) - r0;
+    gemv_item<ACT, R, WT>(a, w, wscale, g, n0, r0, nr, N, K, a_rows, a_src_rows, rows_max, out);
   }
 }
 
@@ -231,6 +262,9 @@ __global__ void __launch_bounds__(kGemvThreads)
 // butterfly, rounded to bf16).  Then out[n] = bf16(sum_j w_j * y_j[n] +
 // shared[n]) with the fp32 adds in slot order, as the combine takes them: the
 // same bits as the two launches, without the round trip of y.
+// With shared_w given, the shared expert's down matmul runs here too: shared[n]
+// = bf16(hs . Wsd[n]) over its K_s, warp j taking the 256-wide K strides j,
+// j + 8, ... (fp32 sums, the lanes by the butterfly, the warps in order).
 constexpr int kTailCols = 4;
 constexpr int kTailSteps = 4;
 constexpr int kTailSlots = kGemvThreads / 32;   // one warp per slot
@@ -242,10 +276,12 @@ __global__ void __launch_bounds__(kGemvThreads)
                              int N, int K, int k,
                              const int32_t* __restrict__ inv_perm, const float* __restrict__ topk_w,
                              const __nv_bfloat16* __restrict__ shared, __nv_bfloat16* __restrict__ out,
-                             int* status) {
+                             int* status, const __nv_bfloat16* __restrict__ shared_w,
+                             const __nv_bfloat16* __restrict__ shared_h, int K_s) {
   __shared__ int s_group[kTailSlots];            // group holding row r (rows <= k), or -1
   __shared__ float s_y[kTailSlots][kTailCols];   // y_j[n], bf16-rounded
   __shared__ int s_live[kTailSlots];
+  __shared__ float s_sh[kTailSlots][kTailCols];  // the shared expert's down, per warp
   using WC = WeightChunk<WT>;
   chain_wait();
   const ChainReleaseAtExit release_next;
@@ -312,13 +348,48 @@ __global__ void __launch_bounds__(kGemvThreads)
       }
     }
   }
+  if (shared_w) {
+    float acc[kTailCols];
+#pragma unroll
+    for (int c = 0; c < kTailCols; ++c) acc[c] = 0.f;
+    for (int kb = warp * 256 + lane * 8; kb < K_s; kb += 256 * kTailSlots) {
+      const uint4 hv = __ldg(reinterpret_cast<const uint4*>(shared_h + kb));
+      uint4 wv[kTailCols];
+#pragma unroll
+      for (int c = 0; c < kTailCols; ++c)
+        wv[c] = __ldg(reinterpret_cast<const uint4*>(shared_w + static_cast<size_t>(n0 + c) * K_s + kb));
+      float af[8];
+      bf16x8(hv, af);
+#pragma unroll
+      for (int c = 0; c < kTailCols; ++c) {
+        float wf[8];
+        bf16x8(wv[c], wf);
+        float s = acc[c];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
+        acc[c] = s;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kTailCols; ++c) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], o);
+      if (lane == 0) s_sh[warp][c] = acc[c];
+    }
+  }
   __syncthreads();
   if (threadIdx.x < kTailCols && n0 + static_cast<int>(threadIdx.x) < N) {
     const int n = n0 + threadIdx.x;
     float v = 0.f;
     for (int s = 0; s < k; ++s)
       if (s_live[s]) v = fmaf(__ldg(topk_w + s), s_y[s][threadIdx.x], v);
-    if (shared) v += __bfloat162float(shared[n]);
+    if (shared_w) {
+      float sh = 0.f;
+      for (int j = 0; j < kTailSlots; ++j) sh += s_sh[j][threadIdx.x];
+      v += __bfloat162float(__float2bfloat16_rn(sh));
+    } else if (shared) {
+      v += __bfloat162float(shared[n]);
+    }
     out[n] = __float2bfloat16_rn(v);
   }
 }
@@ -331,13 +402,16 @@ bool down_combine_gemv_applies(int G, int N, int K, int k) {
 
 int down_combine_gemv_launch(const void* h, const void* w_down, const float* w_scale, const int32_t* offsets, int G,
                              int N, int K, int k, const int32_t* inv_perm, const float* topk_w, const void* shared,
-                             void* out, int* status, cudaStream_t stream, int* launches) {
+                             void* out, int* status, cudaStream_t stream, int* launches, const void* shared_w,
+                             const void* shared_h, int K_s) {
   if (k < 1 || k > kTailSlots || N % kTailCols) return MOE_ERR_UNSUPPORTED;
+  if (shared_w && (!shared_h || K_s <= 0 || K_s % 8)) return MOE_ERR_UNSUPPORTED;
   const dim3 g(N / kTailCols), b(kGemvThreads);
   const cudaError_t rc = launch_chained(
       w_scale ? down_combine_gemv_kernel<1> : down_combine_gemv_kernel<0>, g, b, 0, stream,
       static_cast<const __nv_bfloat16*>(h), static_cast<const uint8_t*>(w_down), w_scale, offsets, G, k, N, K, k,
-      inv_perm, topk_w, static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(out), status);
+      inv_perm, topk_w, static_cast<const __nv_bfloat16*>(shared), static_cast<__nv_bfloat16*>(out), status,
+      static_cast<const __nv_bfloat16*>(shared_w), static_cast<const __nv_bfloat16*>(shared_h), K_s);
   if (rc != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
@@ -349,12 +423,15 @@ bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows) {
 
 int grouped_gemv_launch(const void* a, const void* w, const float* w_scale, const int32_t* offsets, int G,
                         int rows_max, int N, int K, int act, void* out, int* status, cudaStream_t stream,
-                        int* launches, const int32_t* a_rows, int a_src_rows, int max_group_rows, int grid_cap) {
-  if (rows_max == 0) return MOE_OK;
+                        int* launches, const int32_t* a_rows, int a_src_rows, int max_group_rows, int grid_cap,
+                        const void* pre_a, const void* pre_w, int pre_N, void* pre_out) {
+  if (rows_max == 0 && !pre_w) return MOE_OK;
   // at most min(G, rows_max) non-empty groups
   const long long groups = G < rows_max ? G : rows_max;
-  const long long items = groups * (act == 1 ? N : N / kRowsDown);
+  long long items = groups * (act == 1 ? N : N / kRowsDown);
   if (max_group_rows != 1) return MOE_ERR_UNSUPPORTED;
+  if (pre_w && (!pre_a || !pre_out || pre_N <= 0)) return MOE_ERR_UNSUPPORTED;
+  if (pre_w && pre_N > items) items = pre_N;   // the items of the pre-wait matmul go first, on the same warps
   const int form = (act == 1 ? 1 : 0) + (w_scale ? 2 : 0);
   auto kernel = form == 0 ? grouped_gemv_kernel<0, 1, 0>
                           : form == 1 ? grouped_gemv_kernel<1, 1, 0>
@@ -376,9 +453,11 @@ int grouped_gemv_launch(const void* a, const void* w, const float* w_scale, cons
                              (per_sm > 0 ? per_sm : 1);
   if (grid > resident) grid = resident;
   const dim3 g(static_cast<unsigned>(grid)), b(kGemvThreads);
+  const GemvPre pre{static_cast<const __nv_bfloat16*>(pre_a), static_cast<const uint8_t*>(pre_w), pre_N,
+                    static_cast<__nv_bfloat16*>(pre_out)};
   const cudaError_t rc = launch_chained(kernel, g, b, 0, stream, static_cast<const __nv_bfloat16*>(a),
                                         static_cast<const uint8_t*>(w), w_scale, offsets, G, rows_max, N, K, a_rows,
-                                        a_src_rows, static_cast<__nv_bfloat16*>(out), status);
+                                        a_src_rows, static_cast<__nv_bfloat16*>(out), status, pre);
   if (rc != cudaSuccess) return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;

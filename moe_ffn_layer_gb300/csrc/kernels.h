@@ -21,9 +21,11 @@ int route_small_max_tokens();
 // logits_ws: route_ws_bytes(T, H, E) bytes.  ticket: a counter that is zero on
 // entry and left zero (used for T <= route_small_max_tokens(), required there).
 // dispatch != nullptr requires T <= route_small_max_tokens().
+// early_release (T <= 16 form): the launch lets the next kernel of the stream
+// start as soon as its own wait on the previous kernel has returned.
 int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
                  int32_t* topk_ids, float* topk_w, float* logits_ws, unsigned int* ticket, const DispatchOut* dispatch,
-                 int* status, int grid_cap, cudaStream_t stream, int* launches);
+                 int* status, int grid_cap, cudaStream_t stream, int* launches, bool early_release = false);
 
 size_t permute_ws_bytes(int T, int E);
 int permute_launch(const int32_t* topk_ids, const void* x, int T, int H, int E, int k, int32_t* offsets,
@@ -65,17 +67,27 @@ int grouped_gemm_max_groups();
 bool grouped_gemv_applies(int G, int N, int K, int act, int max_group_rows);
 // w_scale non-null: w holds e4m3 codes with one fp32 scale per weight row.
 // grid_cap: SMs the launch may fill (0: all).
+// pre_w non-null: the launch first computes pre_out[1][pre_N] =
+// silu(pre_a . Wg[n]) * (pre_a . Wu[n]) with pre_w = bf16 [2 pre_N][K], before
+// it waits on the previous kernel of the stream; only for a launch whose
+// predecessor lets dependents start once its own wait on its predecessor has
+// returned (route_launch with early_release).
 int grouped_gemv_launch(const void* a, const void* w, const float* w_scale, const int32_t* offsets, int G,
                         int rows_max, int N, int K, int act, void* out, int* status, cudaStream_t stream,
-                        int* launches, const int32_t* a_rows, int a_src_rows, int max_group_rows, int grid_cap = 0);
+                        int* launches, const int32_t* a_rows, int a_src_rows, int max_group_rows, int grid_cap = 0,
+                        const void* pre_a = nullptr, const void* pre_w = nullptr, int pre_N = 0,
+                        void* pre_out = nullptr);
 // One token: gmm2 over its k one-row groups and the combine in one launch
 // (out[H] = bf16(sum_j topk_w[j] * y_j + shared)), the same bits as the one-row
 // gmm2 followed by combine_launch.  h: [k][K] rows in group order; shared
-// nullable.  k <= 8.
+// nullable.  k <= 8.  shared_w non-null (bf16 [N][K_s], K_s % 8 == 0): the
+// shared expert's down matmul of shared_h [K_s] is computed in the same
+// launch and added (rounded to bf16) in place of `shared`.
 bool down_combine_gemv_applies(int G, int N, int K, int k);
 int down_combine_gemv_launch(const void* h, const void* w_down, const float* w_scale, const int32_t* offsets, int G,
                              int N, int K, int k, const int32_t* inv_perm, const float* topk_w, const void* shared,
-                             void* out, int* status, cudaStream_t stream, int* launches);
+                             void* out, int* status, cudaStream_t stream, int* launches,
+                             const void* shared_w = nullptr, const void* shared_h = nullptr, int K_s = 0);
 // logits[T][E] fp32 = x[T][H] . (hi + mid + lo)^T with wr3 = bf16 [E][3H] holding
 // the three bf16 terms of the fp32 router weights in K order (hi | mid | lo);
 // the x tile is re-read for each of the three.  E % 64 == 0, H % 64 == 0.

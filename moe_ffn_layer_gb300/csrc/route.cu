@@ -198,6 +198,7 @@ struct SmallArgs {
   int32_t* offsets;           // nullptr: route only
   int32_t* sorted_token;
   int32_t* inv_perm;
+  int early_release;          // let the next kernel start once this one's wait has returned
 };
 
 // Every CTA: partial logits part[s][t][e] = sum over slice s of H of
@@ -217,6 +218,9 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
   __shared__ int s_off[kMaxExperts];
   __shared__ int s_last, s_total;
   chain_wait();
+  // (early release: the previous kernel has completed, so the next one may
+  // start its work that depends only on what came before this launch)
+  if (a.early_release) chain_release();
   const ChainReleaseAtExit release_next;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, E = a.E, k = a.k, S = a.S;
@@ -295,14 +299,15 @@ int route_small_max_tokens() { return kSmallT; }
 
 int route_launch(const void* x, const float* w_router, const float* bias, int T, int H, int E, int k,
                  int32_t* topk_ids, float* topk_w, float* logits_ws, unsigned int* ticket, const DispatchOut* dispatch,
-                 int* status, int grid_cap, cudaStream_t stream, int* launches) {
+                 int* status, int grid_cap, cudaStream_t stream, int* launches, bool early_release) {
   if (T == 0) return MOE_OK;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (T <= kSmallT) {
     if (!ticket) return MOE_ERR_INVALID;
     const int S = small_slices(H);
     const int grid = (E * S + kSmallThreads / 32 - 1) / (kSmallThreads / 32);
-    SmallArgs a{xb, w_router, bias, T, H, E, k, S, logits_ws, ticket, topk_ids, topk_w, nullptr, nullptr, nullptr};
+    SmallArgs a{xb,      w_router, bias,    T,       H,       E,       k, S, logits_ws, ticket, topk_ids, topk_w,
+                nullptr, nullptr,  nullptr, early_release ? 1 : 0};
     if (dispatch) {
       a.offsets = dispatch->offsets;
       a.sorted_token = dispatch->sorted_token;
