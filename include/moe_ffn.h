@@ -190,9 +190,10 @@ MOE_API int moe_grouped_gemm_noalloc(const void* a, const void* w, const int32_t
  * Other arguments, scratch, checks and the result type as moe_grouped_gemm.
  * Weight-streaming shapes only (the regime whose bytes the format halves):
  * rows_max <= 64 * G, or rows_max == 1; others give MOE_ERR_UNSUPPORTED.  The
- * codes are widened to bf16 in shared memory (exact), multiplied on the
- * tensor cores with fp32 accumulation, and each row's scale is applied to the
- * finished sum. */
+ * codes are widened to bf16 in tensor memory (exact; the NaN codes read as
+ * +-480), multiplied on the tensor cores with fp32 accumulation (on the CUDA
+ * cores for one-row groups), and each row's scale is applied to the finished
+ * sum. */
 MOE_API int moe_grouped_gemm_w8(const void* a, const void* w, const float* w_scale, const int32_t* group_offsets,
                                 int G, int rows_max, int N, int K, int act, void* out, void* ws, size_t ws_bytes,
                                 cudaStream_t stream);
@@ -208,9 +209,11 @@ MOE_API int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const 
 /* The whole layer: route -> permute -> gmm1(+SiLU*mul) -> gmm2 on `stream`;
  * the shared expert's two matmuls on `side` between ev_fork (recorded on
  * `stream`, waited by `side`) and ev_join (recorded on `side`, waited by
- * `stream` before the combine; for one token with k <= 8, gmm2 and the
- * combine are one launch and the join comes before it).  Exactly one fork and
- * one join event per call.
+ * `stream` before the combine).  Exactly one fork and one join event per
+ * call, except for one token (T == 1, k <= 8, H % 4 == 0, I_s % 8 == 0): then
+ * the layer is three launches on `stream` alone (route; gate_up, which also
+ * computes the shared expert's gate_up; down, which also computes the shared
+ * expert's down, and the combine), and `side` and the events go unused.
  * `side` and the events may be NULL when d->I_s == 0.  ws holds every
  * intermediate and the split-K scratch of the four matmuls; size it with
  * moe_workspace_bytes(d, T), align it to 256 bytes and zero-fill it before its
