@@ -81,12 +81,13 @@ constexpr int tmem_cols_pow2(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 
 // WT = 1 (weights-on-M only): the weights are e4m3 codes with one fp32 scale
 // per weight row.  The producer streams the 8-bit weight tiles into a deep
 // ring of their own (the bytes in flight from HBM), limited by nothing but
-// that ring; a token producer warp fills a short token ring (tokens come from
-// L2); eight converter warps widen each 8-bit tile to bf16 (exact: every e4m3
-// value is a bf16 value) straight into tensor memory, where the MMA reads its
-// A operand (a ring of kStages A stages beside the accumulators), so shared
-// memory holds only the 8-bit and token rings; the epilogue multiplies each
-// accumulator row by its scale.
+// that ring; eight converter warps widen each 8-bit tile to bf16 (exact: every
+// e4m3 value is a bf16 value) straight into tensor memory, where the MMA reads
+// its A operand (a ring of kStages A stages beside the accumulators); a token
+// producer warp loads each stage's token tile into the slot of the same index
+// (tokens come from L2), and the converters arrive on a stage once its tokens
+// have landed too, so the MMA thread waits once and commits once per stage;
+// the epilogue multiplies each accumulator row by its scale.
 constexpr int kConvWarps = 8;
 template <int SWAP, int W, int ACT, int MC = 0, int WT = 0>
 struct Cfg {
@@ -94,25 +95,30 @@ struct Cfg {
   static constexpr int kThreads = WT ? 192 + 32 * (kConvWarps + 1) : 192;
   static constexpr int kUnitRows = SWAP ? W : 128;                          // token rows per unit
   static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;
-  static constexpr int kBBytes = W * kBK * 2;
+  // WT: a stage spans kKB 64-wide K blocks (one MMA-thread wait and commit per stage)
+  static constexpr int kKB = WT ? 2 : 1;
+  static constexpr int kBBytes = kKB * W * kBK * 2;                        // token tile(s) of a stage
   static constexpr int kStageBytes = WT ? 0 : kABytes + kBBytes;           // WT: A in tensor memory, tokens apart
-  static constexpr int kStages = WT ? 4 : kSmemBudget / kStageBytes;       // operand stages
-  static constexpr int kTokStages = WT ? 4 : 0;                            // WT: token-tile stages
-  static constexpr int k8Bytes = WT ? (ACT == 1 ? 2 : 1) * 128 * kBK : 0;  // 8-bit weights of a K block
+  static constexpr int kStages = WT ? (ACT == 1 ? 2 : 4) : kSmemBudget / kStageBytes;   // operand stages
+  static constexpr int kTokStages = WT ? kStages : 0;                      // WT: one token slot per A stage
+  // WT: 8-bit weights of a stage: 128 rows x kKB * 64 codes per tile (128-byte rows: the DRAM
+  // reads of a weight row come in 128-byte runs, as in the bf16 form)
+  static constexpr int k8Row = kKB * kBK;
+  static constexpr int k8Bytes = WT ? (ACT == 1 ? 2 : 1) * 128 * k8Row : 0;
   static constexpr int k8Stages =
       WT ? (kSmemBudget - kStages * kStageBytes - kTokStages * kBBytes) / k8Bytes : 0;
   static constexpr int kRingBytes = kStages * kStageBytes + kTokStages * kBBytes + k8Stages * k8Bytes;
   static constexpr int kOutCols = SWAP ? 128 : (ACT == 1 ? W / 2 : W);           // output columns per unit
   static constexpr int kAccCols = SWAP ? (ACT == 1 ? 2 : 1) * W : W;             // TMEM columns per unit
   static constexpr int kNumAcc = 2 * kAccCols <= 512 ? 2 : 1;
-  // WT: tensor-memory columns of one A stage (128 rows x 64 bf16 per tile), after the accumulators
-  static constexpr int kACols = WT ? (ACT == 1 ? 2 : 1) * kBK / 2 : 0;
+  // WT: tensor-memory columns of one A stage (128 rows x kKB * 64 bf16 per tile), after the accumulators
+  static constexpr int kACols = WT ? (ACT == 1 ? 2 : 1) * kKB * kBK / 2 : 0;
   static constexpr int kAColBase = kNumAcc * kAccCols;
   static constexpr int kTmemCols = tmem_cols_pow2(kAColBase + kStages * kACols);
   // after the rings: the mbarriers (full/empty per stage, 2 tfull, 2 tempty,
   // done; with WT full/empty per 8-bit stage and a token barrier per operand
   // stage), the TMEM slot, the abort flag, the unit total and 8 split words
-  static constexpr int kCtrlUsed = (2 * kStages + 5 + 2 * k8Stages + 2 * kTokStages) * 8 + 4 + 4 + 4 + 8 * 4;
+  static constexpr int kCtrlUsed = (2 * kStages + 5 + 2 * k8Stages + kTokStages) * 8 + 4 + 4 + 4 + 8 * 4;
   static constexpr int kCtrlBytes = (kCtrlUsed + 127) / 128 * 128;
   // the carve, from the 1024-aligned base: operand ring | token ring | 8-bit ring | control | group arrays
   static constexpr int kOffTok = kStages * kStageBytes;
@@ -124,6 +130,7 @@ struct Cfg {
   static_assert(kStages >= 2, "ring too shallow");
   static_assert(!WT || (SWAP && !MC && k8Stages >= kTokStages), "8-bit weights: weights-on-M, a deep 8-bit ring");
   static_assert(!WT || kAColBase + kStages * kACols <= 512, "8-bit weights: A stages beside the accumulators");
+  static_assert(!WT || k8Row == 2 * kBK, "8-bit weights: one 128-byte box row per stage (make_map_u8)");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -249,9 +256,8 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   uint64_t* done_bar = tempty_bar + 2;              // [1]
   uint64_t* w8full_bar = done_bar + 1;              // [k8Stages]: 8-bit tile landed
   uint64_t* w8empty_bar = w8full_bar + C::k8Stages; // [k8Stages]: converted
-  uint64_t* tokfull_bar = w8empty_bar + C::k8Stages;   // [kTokStages]: token tile landed
-  uint64_t* tokempty_bar = tokfull_bar + C::kTokStages; // [kTokStages]: its MMAs are done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tokempty_bar + C::kTokStages);
+  uint64_t* tokfull_bar = w8empty_bar + C::k8Stages;   // [kTokStages]: token tile landed (freed with its A stage)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tokfull_bar + C::kTokStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] mode, [1] last arriver, [2..5] warp ok, [6] P, [7] S
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     }
     if (WT) {
       for (int s = 0; s < C::k8Stages; ++s) { mbar_init(&w8full_bar[s], 1); mbar_init(&w8empty_bar[s], kConvWarps); }
-      for (int s = 0; s < C::kTokStages; ++s) { mbar_init(&tokfull_bar[s], 1); mbar_init(&tokempty_bar[s], 1); }
+      for (int s = 0; s < C::kTokStages; ++s) mbar_init(&tokfull_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
     mbar_init(done_bar, 1);
@@ -416,8 +422,9 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
 
   if (warp == 0 && WT) {
     // ------------------------------------------------------------ 8-bit weight producer
-    // lane 0 streams the e4m3 weight tiles (gate and up, or the plain rows;
-    // 128 rows x 64 codes each) into the 8-bit ring, as far ahead as it goes
+    // lane 0 streams the e4m3 weight tiles of each stage (gate and up, or the
+    // plain rows; 128 rows x kKB * 64 codes each) into the 8-bit ring, as far
+    // ahead as it goes
     const uint64_t pol_w = l2_policy_evict_first();
     long long issued = 0;
     int s8 = 0;
@@ -430,12 +437,14 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         int g, row0, nrows, wb, kind;
         decode(pc.u, g, row0, nrows, wb, kind);
         const int wrow = g * wrows + wb * C::kOutCols;
-        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
+        for (int kb = pc.kb0; kb < pc.kb1; kb += C::kKB) {
           if (!mbar_wait(&w8empty_bar[s8], ph8 ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
           uint8_t* dst = w8_base + s8 * C::k8Bytes;
+          // (a stage cut short by the piece's end still loads the whole box: the
+          // codes past the piece are not used, those past K are zero-filled)
           mbar_arrive_expect_tx(&w8full_bar[s8], C::k8Bytes);
           tma_load_2d(dst, &tm_wgt, &w8full_bar[s8], kb * kBK, wrow, pol_w);
-          if (ACT == 1) tma_load_2d(dst + 128 * kBK, &tm_wgt, &w8full_bar[s8], kb * kBK, wrow + args.N, pol_w);
+          if (ACT == 1) tma_load_2d(dst + 128 * C::k8Row, &tm_wgt, &w8full_bar[s8], kb * kBK, wrow + args.N, pol_w);
           ++issued;
           if (++s8 == C::k8Stages) { s8 = 0; ph8 ^= 1u; }
         }
@@ -543,8 +552,8 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0, tstage = 0;
-      uint32_t phase = 0, tphase = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       int it = 0;
       WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
       Piece pc;
@@ -566,38 +575,54 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         if (!mbar_wait(&tempty_bar[ab], aphase ^ 1u, abort_flag, args.status, args.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * C::kAccCols;
+        // the accumulator chains' addresses (gate or plain chains, then up chains)
+        uint32_t dacc[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          dacc[c] = d_tmem + (c & (chains - 1)) * cw;
+          dacc[4 + c] = d_tmem + (chains + (c & (chains - 1))) * cw;
+        }
         const int kb0 = pc.kb0;
         bool ok = true;
-        for (int kb = kb0; kb < pc.kb1; ++kb) {
+        for (int kb = kb0; kb < pc.kb1; kb += C::kKB) {
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
-          if (WT && !mbar_wait(&tokfull_bar[tstage], tphase, abort_flag, args.status, args.wait_ns)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * C::kStageBytes);
-          const uint32_t sb = WT ? smem_u32(tok_base + tstage * C::kBBytes) : sa + C::kABytes;
+          const uint32_t sb = WT ? smem_u32(tok_base + stage * C::kBBytes) : sa + C::kABytes;
           const uint64_t da = smem_desc_k128(sa);
           const uint64_t db = smem_desc_k128(sb);
+          if (WT) {
+            // A from tensor memory: 8 columns per 16-element K step (the up
+            // tile kKB * 32 columns on); B: the stage's token tile of each K
+            // block (W rows x 128 bytes, one after the other).  Every operand
+            // is formed before the first MMA (the issue loop is the bound).
+            const bool full_stage = pc.kb1 - kb >= C::kKB;
+            const uint32_t ta0 = tmem_base + C::kAColBase + stage * C::kACols;
+            uint64_t dbq[C::kKB];
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
+            for (int q = 0; q < C::kKB; ++q) dbq[q] = smem_desc_k128(sb + q * (W * kBK * 2));
+            const bool first = kb == kb0;
+#pragma unroll
+            for (int kk = 0; kk < C::kKB * (kBK / 16); ++kk) {
+              if (kk < kBK / 16 || full_stage) {
+                // (dacc[kk & 3] is chain kk & (chains - 1): chains <= 4)
+                const uint32_t acc = (!first || kk >= chains) ? 1u : 0u;
+                const uint64_t dbk = dbq[kk >> 2] + static_cast<uint64_t>((kk & 3) * 2);
+                umma_bf16_ts(dacc[kk & 3], ta0 + kk * 8, dbk, idesc, acc);
+                if (ACT == 1) umma_bf16_ts(dacc[4 + (kk & 3)], ta0 + C::kKB * kBK / 2 + kk * 8, dbk, idesc, acc);
+              }
+            }
+          }
+          const uint64_t du = smem_desc_k128(sa + kTileRows128);   // (SWAP, SiLU*mul: the up tile)
+#pragma unroll
+          for (int kk = 0; kk < (WT ? 0 : kBK / 16); ++kk) {
             // +32 bytes per 16-element K step inside the 128-byte swizzle row
             const uint64_t ka = static_cast<uint64_t>(kk * 2);
-            if (WT) {
-              // A from tensor memory: 8 columns per 16-element K step; the up tile 32 columns on
-              const int c = kk & (chains - 1);
+            if (SWAP) {
+              // (dacc[kk & 3] is chain kk & (chains - 1): chains <= 4)
               const uint32_t acc = (kb > kb0 || kk >= chains) ? 1u : 0u;
-              const uint32_t ta = tmem_base + C::kAColBase + stage * C::kACols + kk * 8;
-              umma_bf16_ts(d_tmem + c * cw, ta, db + ka, idesc, acc);
-              if (ACT == 1) umma_bf16_ts(d_tmem + (chains + c) * cw, ta + kBK / 2, db + ka, idesc, acc);
-            } else if (SWAP) {
-              const int c = kk & (chains - 1);
-              const uint32_t acc = (kb > kb0 || kk >= chains) ? 1u : 0u;
-              umma_bf16(d_tmem + c * cw, da + ka, db + ka, idesc, acc);
-              if (ACT == 1) {
-                const uint64_t du = smem_desc_k128(sa + kTileRows128);
-                umma_bf16(d_tmem + (chains + c) * cw, du + ka, db + ka, idesc, acc);
-              }
+              umma_bf16(dacc[kk & 3], da + ka, db + ka, idesc, acc);
+              if (ACT == 1) umma_bf16(dacc[4 + (kk & 3)], du + ka, db + ka, idesc, acc);
             } else {
               umma_bf16(d_tmem, da + ka, db + ka, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
             }
@@ -608,10 +633,6 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
           else
             umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-          if (WT) {
-            umma_commit(&tokempty_bar[tstage]);
-            if (++tstage == C::kTokStages) { tstage = 0; tphase ^= 1u; }
-          }
         }
         if (!ok) break;
         umma_commit(&tfull_bar[ab]);           // accumulator ab ready for the epilogue
@@ -855,18 +876,22 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
       }
       bool ok = true;
       if (lane == 0) {
-        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
-          const int kc = kb * kBK;
-          if (!mbar_wait(&tokempty_bar[st], pht ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
-          uint8_t* stok = tok_base + st * C::kBBytes;
-          mbar_arrive_expect_tx(&tokfull_bar[st], static_cast<uint32_t>(nfetch * kBK * 2));
-          if (args.a_rows) {
-            for (int j = 0; j < nfetch; j += 4)
-              tma_gather4(stok + j * kBK * 2, &tm_tok, &tokfull_bar[st], kc, s_gidx[j], s_gidx[j + 1], s_gidx[j + 2],
-                          s_gidx[j + 3], pol_tok);
-          } else {
-            for (int j = 0; j < n16; ++j)
-              tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &tokfull_bar[st], kc, row0 + 16 * j, pol_tok);
+        for (int kb = pc.kb0; kb < pc.kb1; kb += C::kKB) {
+          const int nkb = pc.kb1 - kb < C::kKB ? pc.kb1 - kb : C::kKB;
+          // the slot is free once the MMAs of its A stage's previous use are done
+          if (!mbar_wait(&empty_bar[st], pht ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
+          mbar_arrive_expect_tx(&tokfull_bar[st], static_cast<uint32_t>(nkb * nfetch * kBK * 2));
+          for (int q = 0; q < nkb; ++q) {
+            const int kc = (kb + q) * kBK;
+            uint8_t* stok = tok_base + st * C::kBBytes + q * (W * kBK * 2);
+            if (args.a_rows) {
+              for (int j = 0; j < nfetch; j += 4)
+                tma_gather4(stok + j * kBK * 2, &tm_tok, &tokfull_bar[st], kc, s_gidx[j], s_gidx[j + 1],
+                            s_gidx[j + 2], s_gidx[j + 3], pol_tok);
+            } else {
+              for (int j = 0; j < n16; ++j)
+                tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &tokfull_bar[st], kc, row0 + 16 * j, pol_tok);
+            }
           }
           ++issued;
           if (++st == C::kTokStages) { st = 0; pht ^= 1u; }
@@ -888,15 +913,15 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     // warp may touch only its lane quadrant (warp mod 4), so each thread owns
     // one weight row r of the tile: with gate and up tiles the quadrant's first
     // warp widens the gate row and its second the up row (64 codes -> 32
-    // columns each); a plain tile is split in K halves (32 codes -> 16
-    // columns).  The 8-bit tile comes in the 64-byte swizzle, in which the
-    // 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3), so that the
+    // columns per K block); a plain tile is split in K halves (32 codes -> 16
+    // columns per K block).  The 8-bit tile comes in the 128-byte swizzle, in
+    // which the 16-byte chunk c of row r sits at chunk c ^ (r & 7), so that the
     // row-per-lane reads meet no bank conflicts.  A stage is full when every
-    // converter warp's stores have completed.
+    // converter warp's stores have completed and its token tiles have landed.
     const int quad = warp & 3;
     const int half = (warp - 6) >> 2;
     const int r = quad * 32 + lane;
-    const uint32_t rsw = static_cast<uint32_t>((r >> 1) & 3);
+    const uint32_t rsw = static_cast<uint32_t>(r & 7);
     const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + C::kAColBase;
     int stage = 0, s8 = 0;
     uint32_t phase = 0, ph8 = 0;
@@ -904,18 +929,23 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
     Piece pc;
     while (ok && wi.next(pc)) {
-      for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&w8full_bar[s8], ph8, abort_flag, args.status, args.wait_ns));
-        if (ok)
-          ok = __all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t src = smem_u32(w8_base + s8 * C::k8Bytes) + (ACT == 1 ? half * 128 * kBK : 0) + r * kBK;
-        const uint32_t dst = t_row + stage * C::kACols;
+      for (int kb = pc.kb0; kb < pc.kb1; kb += C::kKB) {
+       const int nkb = pc.kb1 - kb < C::kKB ? pc.kb1 - kb : C::kKB;
+       ok = __all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns));
+       if (!ok) break;
+       tc_fence_after();
+       ok = __all_sync(0xffffffffu, mbar_wait(&w8full_bar[s8], ph8, abort_flag, args.status, args.wait_ns));
+       if (!ok) break;
+       const uint32_t row8 = smem_u32(w8_base + s8 * C::k8Bytes) + (ACT == 1 ? half * 128 * C::k8Row : 0) + r * C::k8Row;
+       // the stage's K blocks: chunks 4q .. 4q + 3 of the row
+       for (int q = 0; q < nkb; ++q) {
+        // gate / up rows: K block q at column q * 32 of the tile's kKB * 32;
+        // plain rows: K block q at column q * 32, this warp's K half 16 on
+        const uint32_t dst = t_row + stage * C::kACols + q * (kBK / 2);
         if (ACT == 1) {
           uint4 v[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = lds_u4(src + ((static_cast<uint32_t>(j) ^ rsw) << 4));
+          for (int j = 0; j < 4; ++j) v[j] = lds_u4(row8 + ((static_cast<uint32_t>(4 * q + j) ^ rsw) << 4));
           uint32_t o[32];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -924,11 +954,11 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
             o[8 * j + 0] = a0.x; o[8 * j + 1] = a0.y; o[8 * j + 2] = a1.x; o[8 * j + 3] = a1.y;
             o[8 * j + 4] = a2.x; o[8 * j + 5] = a2.y; o[8 * j + 6] = a3.x; o[8 * j + 7] = a3.y;
           }
-          tmem_st_32cols(dst + half * (kBK / 2), o);
+          tmem_st_32cols(dst + half * (C::kKB * kBK / 2), o);
         } else {
           uint4 v[2];
 #pragma unroll
-          for (int j = 0; j < 2; ++j) v[j] = lds_u4(src + ((static_cast<uint32_t>(2 * half + j) ^ rsw) << 4));
+          for (int j = 0; j < 2; ++j) v[j] = lds_u4(row8 + ((static_cast<uint32_t>(4 * q + 2 * half + j) ^ rsw) << 4));
           uint32_t o[16];
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
@@ -939,15 +969,18 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
           }
           tmem_st_16cols(dst + half * (kBK / 4), o);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&full_bar[stage]);
-          mbar_arrive(&w8empty_bar[s8]);
-        }
-        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-        if (++s8 == C::k8Stages) { s8 = 0; ph8 ^= 1u; }
+       }
+       tmem_st_wait();
+       __syncwarp();
+       if (lane == 0) mbar_arrive(&w8empty_bar[s8]);   // (its codes have been read and stored)
+       if (++s8 == C::k8Stages) { s8 = 0; ph8 ^= 1u; }
+       // the stage is full once its token tiles have landed too
+       ok = __all_sync(0xffffffffu, mbar_wait(&tokfull_bar[stage], phase, abort_flag, args.status, args.wait_ns));
+       if (!ok) break;
+       tc_fence_before();
+       __syncwarp();
+       if (lane == 0) mbar_arrive(&full_bar[stage]);
+       if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
       }
     }
   }
@@ -995,17 +1028,17 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D byte tensor [rows][cols] (e4m3 weights), box [box_rows][64 bytes], in
-// the 64-byte swizzle (the converter warps read it one row per lane).
+// 2-D byte tensor [rows][cols] (e4m3 weights), box [box_rows][128 bytes], in
+// the 128-byte swizzle (the converter warps read it one row per lane).
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(2 * kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
