@@ -210,7 +210,7 @@ MOE_API int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const 
  * the shared expert's two matmuls on `side` between ev_fork (recorded on
  * `stream`, waited by `side`) and ev_join (recorded on `side`, waited by
  * `stream` before the combine).  Exactly one fork and one join event per
- * call, except for one token (T == 1, k <= 8, H % 4 == 0, I_s % 8 == 0): then
+ * call, except for one token (T == 1, k <= 8, H % 8 == 0, I_s % 8 == 0): then
  * the layer is three launches on `stream` alone (route; gate_up, which also
  * computes the shared expert's gate_up; down, which also computes the shared
  * expert's down, and the combine), and `side` and the events go unused.

@@ -265,8 +265,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 // With shared_w given, the shared expert's down matmul runs here too: shared[n]
 // = bf16(hs . Wsd[n]) over its K_s, warp j taking the 256-wide K strides j,
 // j + 8, ... (fp32 sums, the lanes by the butterfly, the warps in order).
-constexpr int kTailCols = 4;
-constexpr int kTailSteps = 4;
+constexpr int kTailCols = 8;
+constexpr int kTailSteps = 2;
 constexpr int kTailSlots = kGemvThreads / 32;   // one warp per slot
 
 template <int WT>
