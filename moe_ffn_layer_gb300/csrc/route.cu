@@ -10,6 +10,8 @@
 // definition in its benchmark shapes.
 //
 // Kernels:
+//   T == 1    route_cluster: one 8-CTA cluster, a warp per expert over all of H,
+//             the logits gathered in one CTA's shared memory (no ticket).
 //   T <= 16   route_small: one warp per (expert, 512-wide slice of H)
 //             streams its slice of Wr once and dots it with every token; the
 //             CTA that finishes last (a ticket counter) adds the slices in
@@ -26,6 +28,8 @@
 //             to 8 slices of H (the top-k adds the slices in slice order):
 //             below 128 tokens one warp per (expert, slice, 16 tokens), from
 //             128 tokens a 64 x 64 SIMT tile GEMM per slice.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
@@ -260,6 +264,122 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(const SmallA
   if (threadIdx.x == 0) a.offsets[E] = s_total;
 }
 
+// One token (x small enough for shared memory): one cluster of kClCTAs CTAs
+// (16 warps each).  Each warp takes experts w, w + 128, ... (w its index in
+// the cluster) and dots each full Wr row with every token: x is staged in
+// every CTA's shared memory, Wr is streamed from global memory (a lane's 64
+// weights of a 2048-wide chunk of H in flight at once, the warp's first row
+// requested before x is staged).  The logits go straight into the first
+// CTA's shared memory (distributed shared memory); after the cluster barrier
+// that CTA adds the bias, takes the top-k of every token and, in the layer
+// forward, runs the counting sort - the same tail as route_small_kernel,
+// without the partial-logit round trip through global memory and the ticket.
+constexpr int kClCTAs = 8;
+constexpr int kClThreads = 512;
+constexpr int kClWarps = kClCTAs * kClThreads / 32;
+constexpr int kClChunkH = 2048;                 // H per register chunk of a lane (64 fp32 weights)
+constexpr int kClLogitBytes = kSmallT * kMaxExperts * 4;
+constexpr int kClMaxXBytes = 128 * 1024;        // T * H * 2 at most (else route_small_kernel)
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+template <int NPL, int NT>
+__global__ void __launch_bounds__(kClThreads) route_cluster_kernel(const SmallArgs a) {
+  extern __shared__ __align__(16) uint8_t clsm[];
+  float* logit = reinterpret_cast<float*>(clsm);                                   // [T][E], CTA 0's is used
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(clsm + kClLogitBytes);     // [T][H]
+  __shared__ int32_t s_ids[kSmallT * kMaxTopK];
+  __shared__ float s_w[kSmallT * kMaxTopK];
+  __shared__ uint32_t s_mask[kMaxExperts];
+  __shared__ int s_off[kMaxExperts];
+  __shared__ int s_total;
+  // every CTA of the cluster has started before any stores into the first
+  // one's shared memory: arrive now, wait just before the first such store
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  chain_wait();
+  if (a.early_release) chain_release();
+  const ChainReleaseAtExit release_next;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, E = a.E, k = a.k, H = a.H;
+  const uint32_t rank = cluster_ctarank();
+  const int wfirst = static_cast<int>(rank) * (kClThreads / 32) + warp;
+  // a lane's weights of one 2048-wide chunk of a row: h = c + s * 256 + lane * 8 .. + 7, s < 8
+  float4 wv[kClChunkH / 256][2];
+  auto load_w = [&](int e, int c) {
+    const float* row = a.wr + static_cast<size_t>(e) * H + c;
+#pragma unroll
+    for (int s8 = 0; s8 < kClChunkH / 256; ++s8) {
+      const int h = s8 * 256 + lane * 8;
+      if (c + h < H) {
+        wv[s8][0] = __ldg(reinterpret_cast<const float4*>(row + h));
+        wv[s8][1] = __ldg(reinterpret_cast<const float4*>(row + h + 4));
+      } else {
+        wv[s8][0] = wv[s8][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  };
+  if (wfirst < E) load_w(wfirst, 0);
+  // x into this CTA's shared memory
+  for (int i = threadIdx.x; i < T * H / 8; i += kClThreads)
+    reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  const uint32_t logit_addr = smem_u32(logit);
+  for (int e = wfirst; e < E; e += kClWarps) {
+    float acc[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    for (int c = 0; c < H; c += kClChunkH) {
+      if (e != wfirst || c != 0) load_w(e, c);
+#pragma unroll
+      for (int s8 = 0; s8 < kClChunkH / 256; ++s8) {
+        const int h = c + s8 * 256 + lane * 8;
+        if (h < H) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const int tr = t < T ? t : T - 1;   // rows past T repeat the last (their sums are dropped)
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + static_cast<size_t>(tr) * H + h);
+            float f[8];
+            bf16x8_to_f32(xv, f);
+            float v = acc[t];
+            v = fmaf(f[0], wv[s8][0].x, v); v = fmaf(f[1], wv[s8][0].y, v); v = fmaf(f[2], wv[s8][0].z, v);
+            v = fmaf(f[3], wv[s8][0].w, v); v = fmaf(f[4], wv[s8][1].x, v); v = fmaf(f[5], wv[s8][1].y, v);
+            v = fmaf(f[6], wv[s8][1].z, v); v = fmaf(f[7], wv[s8][1].w, v);
+            acc[t] = v;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+      if (lane == t && t < T) st_cluster_f32(logit_addr + static_cast<uint32_t>((t * E + e) * 4), 0u, acc[t]);
+    }
+  }
+  // every logit has landed in the first CTA (the barrier's release / acquire)
+  cluster_sync_all();
+  if (rank != 0) return;
+  if (a.bias)
+    for (int i = threadIdx.x; i < T * E; i += kClThreads) logit[i] += __ldg(a.bias + i % E);
+  __syncthreads();
+  for (int t = warp; t < T; t += kClThreads / 32)
+    warp_topk_softmax<NPL>(logit + t * E, nullptr, E, k, s_ids + t * k, s_w + t * k);
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += kClThreads) {
+    a.topk_ids[i] = s_ids[i];
+    a.topk_w[i] = s_w[i];
+  }
+  if (!a.offsets) return;
+  block_sort_small(s_ids, T, k, E, s_mask, s_off, &s_total, a.sorted_token, a.inv_perm);
+  for (int e = threadIdx.x; e < E; e += kClThreads) a.offsets[e] = s_off[e];
+  if (threadIdx.x == 0) a.offsets[E] = s_total;
+}
+
 template <int NPL>
 cudaError_t launch_small_nt(int nt, int grid, cudaStream_t stream, const SmallArgs& a) {
   const dim3 g(grid), b(kSmallThreads);
@@ -270,6 +390,33 @@ cudaError_t launch_small_nt(int nt, int grid, cudaStream_t stream, const SmallAr
     case 8: return launch_chained(route_small_kernel<NPL, 8>, g, b, 0, stream, a);
     default: return launch_chained(route_small_kernel<NPL, 16>, g, b, 0, stream, a);
   }
+}
+
+// The cluster router's shared-memory attribute, once per (kernel, device).
+template <int NPL, int NT>
+cudaError_t launch_cluster_one(size_t smem, cudaStream_t stream, const SmallArgs& a) {
+  static bool attr_done[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev >= 64 || !attr_done[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(route_cluster_kernel<NPL, NT>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kClLogitBytes + kClMaxXBytes);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) attr_done[dev] = true;
+    }
+  }
+  return launch_chained_cluster(route_cluster_kernel<NPL, NT>, dim3(kClCTAs), dim3(kClThreads), smem, stream,
+                                kClCTAs, a);
+}
+
+cudaError_t launch_cluster(int npl, size_t smem, cudaStream_t stream, const SmallArgs& a) {
+  if (npl == 4) return launch_cluster_one<4, 1>(smem, stream, a);
+  if (npl == 8) return launch_cluster_one<8, 1>(smem, stream, a);
+  return launch_cluster_one<16, 1>(smem, stream, a);
 }
 
 cudaError_t launch_small(int npl, int nt, int grid, cudaStream_t stream, const SmallArgs& a) {
@@ -315,7 +462,16 @@ int route_launch(const void* x, const float* w_router, const float* bias, int T,
     }
     const int nt = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
     const int npl = E <= 128 ? 4 : E <= 256 ? 8 : 16;
-    if (launch_small(npl, nt, grid, stream, a) != cudaSuccess) return MOE_ERR_CUDA;
+    // one token: the one-cluster router (8 SMs, leaving the rest to the launch
+    // that starts beside it); more tokens: the sliced router with its ticket
+    // (a warp's full-H dot per token costs more FMAs than the slices save)
+    const size_t xbytes = static_cast<size_t>(T) * H * 2;
+    if (T == 1 && xbytes <= static_cast<size_t>(kClMaxXBytes) && H % 8 == 0) {
+      if (launch_cluster(npl, kClLogitBytes + align_up(xbytes, 16), stream, a) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else if (launch_small(npl, nt, grid, stream, a) != cudaSuccess) {
+      return MOE_ERR_CUDA;
+    }
     ++*launches;
     return MOE_OK;
   }

@@ -58,6 +58,10 @@ GEMM_CASES = [
     ([1] * 8 + [0] * 100 + [2, 16], 2048, 768, 0),      # decode-like down
     ([100, 0, 5, 200, 1, 63, 65, 0], 384, 256, 1),      # groups over one 64-row chunk
     ([5], 2048, 768, 0),
+    # stages pair the 64-wide K blocks: one block, and an odd count (the last stage half full)
+    ([1, 0, 3, 16, 2, 0, 9, 1], 256, 64, 1),
+    ([1, 0, 3, 16, 2, 0, 9, 1], 384, 320, 0),
+    ([7, 64, 1, 0, 33], 128, 320, 1),
 ]
 
 
