@@ -262,9 +262,10 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
 // butterfly, rounded to bf16).  Then out[n] = bf16(sum_j w_j * y_j[n] +
 // shared[n]) with the fp32 adds in slot order, as the combine takes them: the
 // same bits as the two launches, without the round trip of y.
-// With shared_w given, the shared expert's down matmul runs here too: shared[n]
-// = bf16(hs . Wsd[n]) over its K_s, warp j taking the 256-wide K strides j,
-// j + 8, ... (fp32 sums, the lanes by the butterfly, the warps in order).
+// With shared_w given, the shared expert's down matmul runs here too: warp j
+// computes shared[n0 + j] = bf16(hs . Wsd[n0 + j]) over all of K_s exactly as
+// the one-row matmul does (lanes striding K, fp32 sums, the same butterfly),
+// so the result has the same bits as the standalone launch.
 constexpr int kTailCols = 8;
 constexpr int kTailSteps = 2;
 constexpr int kTailSlots = kGemvThreads / 32;   // one warp per slot
@@ -281,7 +282,8 @@ __global__ void __launch_bounds__(kGemvThreads)
   __shared__ int s_group[kTailSlots];            // group holding row r (rows <= k), or -1
   __shared__ float s_y[kTailSlots][kTailCols];   // y_j[n], bf16-rounded
   __shared__ int s_live[kTailSlots];
-  __shared__ float s_sh[kTailSlots][kTailCols];  // the shared expert's down, per warp
+  __shared__ float s_sh[kTailCols];              // the shared expert's down, column n0 + j from warp j
+  static_assert(kTailCols == kTailSlots, "one warp per column of the shared expert's down");
   using WC = WeightChunk<WT>;
   chain_wait();
   const ChainReleaseAtExit release_next;
@@ -348,34 +350,34 @@ __global__ void __launch_bounds__(kGemvThreads)
       }
     }
   }
-  if (shared_w) {
-    float acc[kTailCols];
+  if (shared_w && n0 + warp < N) {
+    const __nv_bfloat16* wrow = shared_w + static_cast<size_t>(n0 + warp) * K_s;
+    float acc = 0.f;
+    // (eight K strides of loads in flight: one pass for K_s = 2048)
+    constexpr int kShSteps = 8;
+    for (int kb = lane * 8; kb < K_s; kb += 256 * kShSteps) {
+      uint4 hv[kShSteps], wv[kShSteps];
 #pragma unroll
-    for (int c = 0; c < kTailCols; ++c) acc[c] = 0.f;
-    for (int kb = warp * 256 + lane * 8; kb < K_s; kb += 256 * kTailSlots) {
-      const uint4 hv = __ldg(reinterpret_cast<const uint4*>(shared_h + kb));
-      uint4 wv[kTailCols];
+      for (int u = 0; u < kShSteps; ++u) {
+        const int k0 = kb + u * 256;
+        if (k0 < K_s) {
+          hv[u] = __ldg(reinterpret_cast<const uint4*>(shared_h + k0));
+          wv[u] = __ldg(reinterpret_cast<const uint4*>(wrow + k0));
+        }
+      }
 #pragma unroll
-      for (int c = 0; c < kTailCols; ++c)
-        wv[c] = __ldg(reinterpret_cast<const uint4*>(shared_w + static_cast<size_t>(n0 + c) * K_s + kb));
-      float af[8];
-      bf16x8(hv, af);
+      for (int u = 0; u < kShSteps; ++u) {
+        if (kb + u * 256 >= K_s) break;
+        float af[8], wf[8];
+        bf16x8(hv[u], af);
+        bf16x8(wv[u], wf);
 #pragma unroll
-      for (int c = 0; c < kTailCols; ++c) {
-        float wf[8];
-        bf16x8(wv[c], wf);
-        float s = acc[c];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s = fmaf(af[e], wf[e], s);
-        acc[c] = s;
+        for (int e = 0; e < 8; ++e) acc = fmaf(af[e], wf[e], acc);
       }
     }
 #pragma unroll
-    for (int c = 0; c < kTailCols; ++c) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], o);
-      if (lane == 0) s_sh[warp][c] = acc[c];
-    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) s_sh[warp] = acc;
   }
   __syncthreads();
   if (threadIdx.x < kTailCols && n0 + static_cast<int>(threadIdx.x) < N) {
@@ -384,9 +386,7 @@ __global__ void __launch_bounds__(kGemvThreads)
     for (int s = 0; s < k; ++s)
       if (s_live[s]) v = fmaf(__ldg(topk_w + s), s_y[s][threadIdx.x], v);
     if (shared_w) {
-      float sh = 0.f;
-      for (int j = 0; j < kTailSlots; ++j) sh += s_sh[j][threadIdx.x];
-      v += __bfloat162float(__float2bfloat16_rn(sh));
+      v += __bfloat162float(__float2bfloat16_rn(s_sh[threadIdx.x]));
     } else if (shared) {
       v += __bfloat162float(shared[n]);
     }
