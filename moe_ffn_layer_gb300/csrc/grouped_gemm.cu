@@ -94,11 +94,13 @@ struct Cfg {
   // 6 warps (+ the converter warps and the token producer warp)
   static constexpr int kThreads = WT ? 192 + 32 * (kConvWarps + 1) : 192;
   static constexpr int kUnitRows = SWAP ? W : 128;                          // token rows per unit
-  static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;
-  // WT: a stage spans kKB 64-wide K blocks (one MMA-thread wait and commit per stage)
-  static constexpr int kKB = WT ? 2 : 1;
+  static constexpr int kABytes = SWAP ? (ACT == 1 ? 2 : 1) * kTileRows128 : kTileRows128;   // per K block
+  // weights-on-M: a stage spans kKB 64-wide K blocks (one MMA-thread wait and
+  // commit per kKB * 4 K steps: the small-N MMAs' issue thread is the bound)
+  static constexpr int kKB = SWAP ? 2 : 1;
   static constexpr int kBBytes = kKB * W * kBK * 2;                        // token tile(s) of a stage
-  static constexpr int kStageBytes = WT ? 0 : kABytes + kBBytes;           // WT: A in tensor memory, tokens apart
+  // WT: A in tensor memory, tokens apart; else A tiles of the stage's K blocks, then their token tiles
+  static constexpr int kStageBytes = WT ? 0 : kKB * kABytes + kBBytes;
   static constexpr int kStages = WT ? (ACT == 1 ? 2 : 4) : kSmemBudget / kStageBytes;   // operand stages
   static constexpr int kTokStages = WT ? kStages : 0;                      // WT: one token slot per A stage
   // WT: 8-bit weights of a stage: 128 rows x kKB * 64 codes per tile (128-byte rows: the DRAM
@@ -484,17 +486,38 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
                                                    nfetch * kBK * 2);
       bool ok = true;
       if (lane == 0) {
-        for (int kb = pc.kb0; kb < pc.kb1; ++kb) {
+        for (int kb = pc.kb0; kb < pc.kb1; kb += C::kKB) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
           uint8_t* sa = stage_base + stage * C::kStageBytes;
-          uint8_t* sb = sa + C::kABytes;
+          uint8_t* sb = sa + C::kKB * C::kABytes;
           const int kc = kb * kBK;
-          mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          uint8_t* stok = SWAP ? sb : sa;   // where the token rows go
           if (SWAP) {
-            tma_load_2d(sa, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
-            if (ACT == 1) tma_load_2d(sa + kTileRows128, &tm_wgt, &full_bar[stage], kc, wrow + args.N, pol_w);
-          } else if (MC) {
+            // the stage's K blocks: weight tile(s) of block q at sa + q * kABytes, its token rows at
+            // sb + q * (W rows x 128 bytes)
+            const int nkb = pc.kb1 - kb < C::kKB ? pc.kb1 - kb : C::kKB;
+            mbar_arrive_expect_tx(&full_bar[stage], nkb * bytes);
+            for (int q = 0; q < nkb; ++q) {
+              const int kq = kc + q * kBK;
+              uint8_t* aq = sa + q * C::kABytes;
+              uint8_t* bq = sb + q * (W * kBK * 2);
+              tma_load_2d(aq, &tm_wgt, &full_bar[stage], kq, wrow, pol_w);
+              if (ACT == 1) tma_load_2d(aq + kTileRows128, &tm_wgt, &full_bar[stage], kq, wrow + args.N, pol_w);
+              if (args.a_rows) {
+                for (int j = 0; j < nfetch; j += 4)
+                  tma_gather4(bq + j * kBK * 2, &tm_tok, &full_bar[stage], kq, s_gidx[j], s_gidx[j + 1],
+                              s_gidx[j + 2], s_gidx[j + 3], pol_tok);
+              } else {
+                for (int j = 0; j < n16; ++j)
+                  tma_load_2d(bq + j * 16 * kBK * 2, &tm_tok, &full_bar[stage], kq, row0 + 16 * j, pol_tok);
+              }
+            }
+            ++issued;
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+            continue;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          uint8_t* stok = sa;   // (tokens-on-M: the token rows go first)
+          if (MC) {
             // weight rows in two 128-row halves: gate | up with SiLU*mul, else rows
             // 0..127 | 128..255 of the block; a weight-sharing pair loads one half
             // per CTA, to both
@@ -518,9 +541,6 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
             for (int j = 0; j < nfetch; j += 4)
               tma_gather4(stok + j * kBK * 2, &tm_tok, &full_bar[stage], kc, s_gidx[j], s_gidx[j + 1],
                           s_gidx[j + 2], s_gidx[j + 3], pol_tok);
-          } else if (SWAP) {
-            for (int j = 0; j < n16; ++j)
-              tma_load_2d(stok + j * 16 * kBK * 2, &tm_tok, &full_bar[stage], kc, row0 + 16 * j, pol_tok);
           } else if (MC) {
             // token rows in two 64-row halves; a token-sharing pair loads one half
             // per CTA, to both
@@ -588,7 +608,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, args.status, args.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(stage_base + stage * C::kStageBytes);
-          const uint32_t sb = WT ? smem_u32(tok_base + stage * C::kBBytes) : sa + C::kABytes;
+          const uint32_t sb = WT ? smem_u32(tok_base + stage * C::kBBytes) : sa + C::kKB * C::kABytes;
           const uint64_t da = smem_desc_k128(sa);
           const uint64_t db = smem_desc_k128(sb);
           if (WT) {
@@ -613,17 +633,34 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
               }
             }
           }
-          const uint64_t du = smem_desc_k128(sa + kTileRows128);   // (SWAP, SiLU*mul: the up tile)
+          if (SWAP && !WT) {
+            // the stage's K blocks q: weight tile(s) at sa + q * kABytes, token rows at
+            // sb + q * (W rows x 128 bytes); every operand formed before the first MMA
+            const bool full_stage = pc.kb1 - kb >= C::kKB;
+            uint64_t daq[C::kKB], duq[C::kKB], dbq[C::kKB];
 #pragma unroll
-          for (int kk = 0; kk < (WT ? 0 : kBK / 16); ++kk) {
+            for (int q = 0; q < C::kKB; ++q) {
+              daq[q] = smem_desc_k128(sa + q * C::kABytes);
+              duq[q] = smem_desc_k128(sa + q * C::kABytes + kTileRows128);
+              dbq[q] = smem_desc_k128(sb + q * (W * kBK * 2));
+            }
+            const bool first = kb == kb0;
+#pragma unroll
+            for (int kk = 0; kk < C::kKB * (kBK / 16); ++kk) {
+              if (kk < kBK / 16 || full_stage) {
+                // (dacc[kk & 3] is chain kk & (chains - 1): chains <= 4; +32 bytes per K step)
+                const uint32_t acc = (!first || kk >= chains) ? 1u : 0u;
+                const uint64_t ka = static_cast<uint64_t>((kk & 3) * 2);
+                umma_bf16(dacc[kk & 3], daq[kk >> 2] + ka, dbq[kk >> 2] + ka, idesc, acc);
+                if (ACT == 1) umma_bf16(dacc[4 + (kk & 3)], duq[kk >> 2] + ka, dbq[kk >> 2] + ka, idesc, acc);
+              }
+            }
+          }
+#pragma unroll
+          for (int kk = 0; kk < (SWAP ? 0 : kBK / 16); ++kk) {
             // +32 bytes per 16-element K step inside the 128-byte swizzle row
             const uint64_t ka = static_cast<uint64_t>(kk * 2);
-            if (SWAP) {
-              // (dacc[kk & 3] is chain kk & (chains - 1): chains <= 4)
-              const uint32_t acc = (kb > kb0 || kk >= chains) ? 1u : 0u;
-              umma_bf16(dacc[kk & 3], da + ka, db + ka, idesc, acc);
-              if (ACT == 1) umma_bf16(dacc[4 + (kk & 3)], du + ka, db + ka, idesc, acc);
-            } else {
+            {
               umma_bf16(d_tmem, da + ka, db + ka, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
             }
           }
