@@ -22,25 +22,35 @@ namespace {
 constexpr int kTB = 256;            // tokens per block (threads per block)
 constexpr int kMaskWords = kTB / 32;
 
-// Validates token t's ids (in [0,E), pairwise distinct) and ORs its bits into
-// the block mask.  Returns false (and records the error) for a bad token.
-__device__ __forceinline__ bool mask_token(const int32_t* ids, int t, int tl, int E, int k, uint32_t* mask,
+// Token t's k expert ids in registers, every load issued at once (slots past
+// k hold -1): one memory round trip instead of one per slot.
+__device__ __forceinline__ void load_ids(const int32_t* __restrict__ ids, int t, int k, int (&e)[kMaxTopK]) {
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) e[j] = j < k ? ids[static_cast<size_t>(t) * k + j] : -1;
+}
+
+// Validates a token's ids (in [0,E), pairwise distinct) and ORs its bit (local
+// token tl) into the block mask.  Returns false (and records the error) for a
+// bad token.
+__device__ __forceinline__ bool mask_token(const int (&e)[kMaxTopK], int tl, int E, int k, uint32_t* mask,
                                            int* status) {
   bool ok = true;
-  for (int j = 0; j < k; ++j) {
-    const int e = ids[static_cast<size_t>(t) * k + j];
-    if (e < 0 || e >= E) ok = false;
-    for (int i = 0; i < j; ++i)
-      if (ids[static_cast<size_t>(t) * k + i] == e) ok = false;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j < k) {
+      if (e[j] < 0 || e[j] >= E) ok = false;
+#pragma unroll
+      for (int i = 0; i < j; ++i)
+        if (e[i] == e[j]) ok = false;
+    }
   }
   if (!ok) {
     set_status(status, MOE_ERR_DEVICE_CHECK);
     return false;
   }
-  for (int j = 0; j < k; ++j) {
-    const int e = ids[static_cast<size_t>(t) * k + j];
-    atomicOr(&mask[e * kMaskWords + (tl >> 5)], 1u << (tl & 31));
-  }
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) atomicOr(&mask[e[j] * kMaskWords + (tl >> 5)], 1u << (tl & 31));
   return true;
 }
 
@@ -101,9 +111,11 @@ __global__ void __launch_bounds__(kTB)
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int t = threadIdx.x;
+  int ev[kMaxTopK];
+  load_ids(ids, t < T ? t : 0, k, ev);
   for (int i = t; i < E * kMaskWords; i += kTB) mask[i] = 0;
   __syncthreads();
-  const bool valid = t < T && mask_token(ids, t, t, E, k, mask, status);
+  const bool valid = t < T && mask_token(ev, t, E, k, mask, status);
   __syncthreads();
   for (int e = t; e < E; e += kTB) s_off[e] = mask_count(mask, e);
   __syncthreads();
@@ -111,10 +123,11 @@ __global__ void __launch_bounds__(kTB)
   for (int e = t; e < E; e += kTB) offsets[e] = s_off[e];
   if (t == 0) offsets[E] = total;
   if (t < T) {
-    for (int j = 0; j < k; ++j) {
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) continue;
       if (valid) {
-        const int e = ids[static_cast<size_t>(t) * k + j];
-        const int r = s_off[e] + mask_rank(mask, e, t);
+        const int r = s_off[ev[j]] + mask_rank(mask, ev[j], t);
         sorted_token[r] = t;
         inv_perm[static_cast<size_t>(t) * k + j] = r;
       } else {
@@ -132,9 +145,11 @@ __global__ void __launch_bounds__(kTB)
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int tl = threadIdx.x, t = blockIdx.x * kTB + tl;
+  int ev[kMaxTopK];
+  load_ids(ids, t < T ? t : 0, k, ev);
   for (int i = tl; i < E * kMaskWords; i += kTB) mask[i] = 0;
   __syncthreads();
-  if (t < T) mask_token(ids, t, tl, E, k, mask, status);
+  if (t < T) mask_token(ev, tl, E, k, mask, status);
   __syncthreads();
   for (int e = tl; e < E; e += kTB) block_counts[static_cast<size_t>(blockIdx.x) * E + e] = mask_count(mask, e);
 }
@@ -154,6 +169,8 @@ __global__ void __launch_bounds__(kTB)
   const ChainReleaseAtExit release_next;
   const int tl = threadIdx.x, t = blockIdx.x * kTB + tl;
   const int b = blockIdx.x, B = gridDim.x;
+  int ev[kMaxTopK];
+  load_ids(ids, t < T ? t : 0, k, ev);
   for (int i = tl; i < E * kMaskWords; i += kTB) mask[i] = 0;
   for (int e = tl; e < E; e += kTB) {
     int before = 0, tot = 0;
@@ -168,16 +185,18 @@ __global__ void __launch_bounds__(kTB)
   }
   __syncthreads();
   // errors were recorded by the count pass
-  const bool valid = t < T && mask_token(ids, t, tl, E, k, mask, nullptr);
+  const bool valid = t < T && mask_token(ev, tl, E, k, mask, nullptr);
   const int total = block_exclusive_scan(s_tot, E);   // s_tot -> offsets
   if (b == 0) {
     for (int e = tl; e < E; e += kTB) offsets[e] = s_tot[e];
     if (tl == 0) offsets[E] = total;
   }
   if (t >= T) return;
-  for (int j = 0; j < k; ++j) {
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j >= k) continue;
     if (valid) {
-      const int e = ids[static_cast<size_t>(t) * k + j];
+      const int e = ev[j];
       const int r = s_tot[e] + s_before[e] + mask_rank(mask, e, tl);
       sorted_token[r] = t;
       inv_perm[static_cast<size_t>(t) * k + j] = r;
@@ -189,7 +208,12 @@ __global__ void __launch_bounds__(kTB)
 
 // x_perm[inv_perm[t*k + j]] = x[t]: one warp per token reads its row once (16-byte
 // loads) and writes its k copies, so x is read from memory once even when it
-// does not fit in L2.  Pairs the sort rejected (row -1) are skipped.
+// does not fit in L2.  A lane issues the loads of up to kRowChunk of its
+// 16-byte pieces before the first store (one memory round trip per 2048
+// bf16 of H instead of one per 256).  Pairs the sort rejected (row -1) are
+// skipped.
+constexpr int kRowChunk = 8;
+
 __global__ void __launch_bounds__(256)
     scatter_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv_perm, int T, int H, int k,
                         long long rows_max, uint4* __restrict__ x_perm) {
@@ -205,11 +229,21 @@ __global__ void __launch_bounds__(256)
       dst[j] = (r >= 0 && r < rows_max) ? r : -1;
     }
     const uint4* src = x + static_cast<size_t>(t) * vec;
-    for (int i = lane; i < vec; i += 32) {
-      const uint4 v = __ldg(src + i);
+    for (int i0 = 0; i0 < vec; i0 += 32 * kRowChunk) {
+      uint4 v[kRowChunk];
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
-        if (dst[j] >= 0) x_perm[static_cast<size_t>(dst[j]) * vec + i] = v;
+      for (int c = 0; c < kRowChunk; ++c) {
+        const int i = i0 + c * 32 + lane;
+        if (i < vec) v[c] = __ldg(src + i);
+      }
+#pragma unroll
+      for (int c = 0; c < kRowChunk; ++c) {
+        const int i = i0 + c * 32 + lane;
+        if (i >= vec) continue;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+          if (dst[j] >= 0) x_perm[static_cast<size_t>(dst[j]) * vec + i] = v[c];
+      }
     }
   }
 }

@@ -203,6 +203,10 @@ GEMM_CASES = [
     ([128, 1, 255, 0, 257], 128, 256, 1),
     ([64, 1000], 192, 64, 1),
     ([513], 512, 128, 0),
+    # multicast pairs over several weight blocks: single tiles, odd last tiles
+    # beside tile pairs, an odd number of weight-block pairs
+    ([127, 129, 0, 300, 385], 768, 128, 1),
+    ([257, 0, 384, 1], 1024, 192, 0),
 ]
 
 
