@@ -213,7 +213,11 @@ MOE_API int moe_unpermute_combine(const void* y, const int32_t* inv_perm, const 
  * call, except for one token (T == 1, k <= 8, H % 8 == 0, I_s % 8 == 0): then
  * the layer is three launches on `stream` alone (route; gate_up, which also
  * computes the shared expert's gate_up; down, which also computes the shared
- * expert's down, and the combine), and `side` and the events go unused.
+ * expert's down, and the combine), and `side` and the events go unused; and
+ * for 4 to 9 tokens with bf16 routed weights (I, H, I_s multiples of 128,
+ * T*k <= 64*E): four launches on `stream` alone (route with the dispatch;
+ * gate_up, led by the shared expert's gate_up; down, led by the shared
+ * expert's down; combine), again without `side` or the events.
  * `side` and the events may be NULL when d->I_s == 0.  ws holds every
  * intermediate and the split-K scratch of the four matmuls; size it with
  * moe_workspace_bytes(d, T), align it to 256 bytes and zero-fill it before its

@@ -31,6 +31,11 @@ thread_local int t_last_launches = 0;
 // T=16384, E=256, H=4096) leaves enough idle SMs of its own that forking
 // before it is better (4507 -> 4403 us there; the T=8192, E=128 prefill loses
 // 759 -> 791 us).
+// Batches whose shared expert runs as the leading phase of the routed matmul
+// launches (see forward_impl).
+constexpr int kLeadMinT = 4;
+constexpr int kLeadMaxT = 9;
+
 int fork_stage(const moe_dims* d, int T) {
   return static_cast<double>(T) * d->E * d->H >= 8589934592.0 ? 0 : 1;
 }
@@ -397,12 +402,26 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
   const bool one_token_fused = T == 1 && has_shared && d->I_s % 8 == 0 &&
                                moe::down_combine_gemv_applies(d->E, d->H, d->I, d->k) &&
                                moe::grouped_gemv_applies(d->E, d->I, d->H, 1, 1);
+  // 4 to 9 tokens with a shared expert (bf16 weights): no side stream either.
+  // The routed matmul launches carry the shared expert as a leading phase:
+  // its gate_up streams the shared weights while the router runs (before that
+  // launch's wait on the router), its down leads the routed down launch, and
+  // the combine adds its row.  Every SM serves both.  Measured against the
+  // side stream (decode sizes, one GPU, back to back): 2.3 us faster on
+  // average over T = 4..9 (T = 8: 111.7 -> 109.2 us), slower at T = 2, 3 and
+  // from 12 on, where the routing window is too short to hide the shared
+  // gate_up or the larger router leaves no room beside it on its SMs.
+  const bool lead_shared = !one_token_fused && T >= kLeadMinT && T <= kLeadMaxT && has_shared &&
+                           !w->s_gate_up && L.gemm_side_bytes > 0 &&
+                           moe::lead_phase_applies(T, d->I_s, d->H) && moe::lead_phase_applies(T, d->H, d->I_s) &&
+                           moe::grouped_gemm_weights_on_m(d->E, rows, d->I) &&
+                           moe::grouped_gemm_weights_on_m(d->E, rows, d->H);
   // SMs for the two streams.  At decode sizes both are weight streams that
   // run side by side for the whole call: the shared expert gets the SMs in
   // proportion to its share of the weight bytes (at least 8, at most half),
   // the routed matmuls the rest.  Larger batches give both streams every SM.
   int side_sms = di->sms, main_sms = di->sms;
-  if (T <= moe::route_small_max_tokens() && has_shared && !one_token_fused) {
+  if (T <= moe::route_small_max_tokens() && has_shared && !one_token_fused && !lead_shared) {
     const double shared_bytes = 3.0 * d->I_s * d->H * 2;
     const double routed_bytes = 3.0 * d->I * d->H * 2 * std::min<long long>(d->E, static_cast<long long>(T) * d->k);
     int c = static_cast<int>(di->sms * shared_bytes / (shared_bytes + routed_bytes) + 0.5);
@@ -428,13 +447,13 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
   if (T <= moe::route_small_max_tokens()) {
     // decode sizes: the shared expert streams its weights while one router
     // launch routes and dispatches
-    if (!one_token_fused) rc = fork_shared();
+    if (!one_token_fused && !lead_shared) rc = fork_shared();
     // router, top-k and counting sort in one launch
     const moe::DispatchOut dout{offsets, sorted, inv};
     if (!rc)
       rc = moe::route_launch(x, w->w_router, w->router_bias, T, d->H, d->E, d->k, ids, tw, logits,
                              reinterpret_cast<unsigned int*>(base + L.route_ticket), &dout, di->status, di->sms,
-                             stream, &n, one_token_fused);
+                             stream, &n, one_token_fused || lead_shared);
   } else {
     const int fork_at = fork_stage(d, T);
     if (fork_at == 0) rc = fork_shared();
@@ -447,6 +466,8 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
                                di->sms, stream, &n);
     if (!rc && fork_at == 2) rc = fork_shared();
   }
+  const moe::LeadPhase lead_gu{x, w->ws_gate_up, T, d->I_s, d->H, hs, true, gside};
+  const moe::LeadPhase lead_dn{hs, w->ws_down, T, d->H, d->I_s, s, false, gside};
   if (!rc)
     // decode sizes: gmm1 reads the dispatched rows straight from x through
     // sorted_token (TMA gather4, a few rows per stage); larger batches read the
@@ -457,7 +478,8 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
                                         di->status, stream, &n, sorted, T, 1, di->sms, x, w->ws_gate_up, d->I_s, hs)
          : T <= moe::route_small_max_tokens()
              ? moe::grouped_gemm_launch(x, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status, &gmain,
-                                        main_sms, stream, &n, sorted, T, 0, T, w->s_gate_up)
+                                        main_sms, stream, &n, sorted, T, 0, T, w->s_gate_up,
+                                        lead_shared ? &lead_gu : nullptr)
              : moe::grouped_gemm_launch(xperm, w->w_gate_up, offsets, d->E, rows, d->I, d->H, 1, h, di->status,
                                         &gmain, di->sms, stream, &n, nullptr, 0, 0, 0, w->s_gate_up);
   // one token: gmm2 and the combine in one launch, after the join (the shared
@@ -465,10 +487,11 @@ int forward_impl(const moe_dims* d, const LayerWeights* w, const void* x, int T,
   const bool fused_tail = T == 1 && moe::down_combine_gemv_applies(d->E, d->H, d->I, d->k);
   if (!rc && !fused_tail)
     rc = moe::grouped_gemm_launch(h, w->w_down, offsets, d->E, rows, d->H, d->I, 0, y, di->status, &gmain,
-                                  main_sms, stream, &n, nullptr, 0, 0, T, w->s_down);
+                                  main_sms, stream, &n, nullptr, 0, 0, T, w->s_down, lead_shared ? &lead_dn : nullptr);
   if (rc) return rc;
   // join, then combine
-  if (has_shared && !one_token_fused && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  if (has_shared && !one_token_fused && !lead_shared && cudaStreamWaitEvent(stream, ev_join, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
   rc = fused_tail ? moe::down_combine_gemv_launch(h, w->w_down, w->s_down, offsets, d->E, d->H, d->I, d->k, inv, tw,
                                                   has_shared && !one_token_fused ? s : nullptr, out, di->status,
                                                   stream, &n, one_token_fused ? w->ws_down : nullptr,

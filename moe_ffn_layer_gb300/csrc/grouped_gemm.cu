@@ -120,7 +120,7 @@ struct Cfg {
   // after the rings: the mbarriers (full/empty per stage, 2 tfull, 2 tempty,
   // done; with WT full/empty per 8-bit stage and a token barrier per operand
   // stage), the TMEM slot, the abort flag, the unit total and 8 split words
-  static constexpr int kCtrlUsed = (2 * kStages + 5 + 2 * k8Stages + kTokStages) * 8 + 4 + 4 + 4 + 8 * 4;
+  static constexpr int kCtrlUsed = (2 * kStages + 6 + 2 * k8Stages + kTokStages) * 8 + 4 + 4 + 4 + 8 * 4;
   static constexpr int kCtrlBytes = (kCtrlUsed + 127) / 128 * 128;
   // the carve, from the 1024-aligned base: operand ring | token ring | 8-bit ring | control | group arrays
   static constexpr int kOffTok = kStages * kStageBytes;
@@ -159,6 +159,22 @@ struct GemmArgs {
                            // (fetched with TMA gather4; no permuted copy needed)
   uint64_t wait_ns;        // limit of every bounded wait but the drains (0: expire at once)
   const float* wscale;     // 8-bit weights: one scale per weight row ([G][rows of W[g]])
+  // a leading phase (weights-on-M, bf16): one group of pre_rows <= 16 token rows
+  // with operands of its own (tensor maps tm_tok2 / tm_wgt2), K = pre_K, output
+  // pre_out [pre_rows][pre_N], split-K scratch of its own; pre_early: it runs
+  // before the kernel waits on the previous one (its operands do not come from it)
+  int pre_units;           // 0: no leading phase
+  int pre_N, pre_K, pre_rows, pre_early;
+  __nv_bfloat16* pre_out;
+  int* pre_counters;       // >= pre_units tickets, zero between calls (nullptr: no split)
+  float* pre_partials;
+  int pre_split_cap;
+};
+
+// A phase of a launch: its units, K blocks and split plan; pre = the leading phase.
+struct Phase {
+  int mode, S, P, units, kblocks;
+  bool pre;
 };
 
 // fp32 values one TMEM lane keeps per split-K partial
@@ -236,9 +252,38 @@ struct WorkIter {
 // last arriver's sum), in K blocks; measured on decode shapes.
 constexpr int kPieceCost = 6;
 
+// Split plan of a phase whose groups all hold <= kSplitRows rows: the cheapest
+// of S-way splits (S = 1, 2, 4, 8) and stream-K, costed as the longest CTA's K
+// blocks plus kPieceCost per piece it runs; P = the most pieces one unit can
+// be cut into.
+__device__ void choose_split(int units, int kblocks, int grid, long long split_cap, int& mode, int& S, int& P) {
+  mode = 0;
+  S = 1;
+  P = 1;
+  long long best = static_cast<long long>((units + grid - 1) / grid) * (kblocks + kPieceCost);
+  for (int c = 2; c <= kMaxSplit; c *= 2) {
+    if (kblocks % c || static_cast<long long>(units) * c > split_cap) continue;
+    const long long cost = ((static_cast<long long>(units) * c + grid - 1) / grid) * (kblocks / c + kPieceCost);
+    if (cost < best) { best = cost; S = c; P = c; }
+  }
+  const long long tot = static_cast<long long>(units) * kblocks;
+  const long long share = tot / grid;
+  if (share >= 1) {
+    const int psk = static_cast<int>((kblocks + share - 1) / share) + 1;
+    const long long pieces_per_cta = (share + kblocks - 1) / kblocks + 1;
+    const long long cost = (tot + grid - 1) / grid + kPieceCost * pieces_per_cta;
+    if (cost < best && static_cast<long long>(units) * psk <= split_cap) {
+      mode = 1;
+      S = 1;
+      P = psk;
+    }
+  }
+}
+
 template <int SWAP, int W, int ACT, int MC = 0, int WT = 0>
 __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_tok, const __grid_constant__ CUtensorMap tm_wgt,
+                        const __grid_constant__ CUtensorMap tm_tok2, const __grid_constant__ CUtensorMap tm_wgt2,
                         const GemmArgs args) {
   static_assert(!MC || (!SWAP && W == 256 && (ACT == 0 || ACT == 1)), "pairs: tokens-on-M, 256-wide blocks");
   constexpr int kTokHalf = 64 * kBK * 2;   // bytes of 64 token rows of a K block
@@ -259,7 +304,8 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   uint64_t* w8full_bar = done_bar + 1;              // [k8Stages]: 8-bit tile landed
   uint64_t* w8empty_bar = w8full_bar + C::k8Stages; // [k8Stages]: converted
   uint64_t* tokfull_bar = w8empty_bar + C::k8Stages;   // [kTokStages]: token tile landed (freed with its A stage)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tokfull_bar + C::kTokStages);
+  uint64_t* table_bar = tokfull_bar + C::kTokStages;  // [1]: unit table built (after a leading phase)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(table_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_split = reinterpret_cast<int*>(tmem_slot + 3);   // [0] mode, [1] last arriver, [2..5] warp ok, [6] P, [7] S
@@ -288,6 +334,8 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
     mbar_init(done_bar, 1);
+    mbar_init(table_bar, 1);
+    *abort_flag = 0;
     fence_barrier_init();
   } else if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_tok);
@@ -298,15 +346,20 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   const int crank = MC ? static_cast<int>(cluster_ctarank()) : 0;
   const int wgrid = MC ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);   // work lists
   const int wcta = MC ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
-  chain_wait();
+  // A leading phase that needs nothing from the previous kernel runs before
+  // the wait on it: then the producer alone waits, builds the unit table and
+  // publishes it (table_bar); otherwise every thread waits first.
+  const bool pre = SWAP && !WT && args.pre_units > 0;
+  const bool deferred = pre && args.pre_early != 0;
+  if (!deferred) chain_wait();
   const ChainReleaseAtExit release_next;
-  // ---- group offsets into shared memory (all threads)
-  for (int i = threadIdx.x; i <= G; i += kThreads)
-    s_off[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows_max);
-  __syncthreads();
   const int kblocks = args.K / kBK;
   // ---- unit table (warp 0): checks, unit prefix per group, split choice
-  if (warp == 0) {
+  auto build_table = [&]() {
+    if (deferred) {   // (otherwise every thread has loaded the offsets)
+      for (int i = lane; i <= G; i += 32) s_off[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows_max);
+      __syncwarp();
+    }
     const int per = (G + 31) / 32;
     const int g0 = lane * per;
     int local = 0, mx = 0;
@@ -337,46 +390,41 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     const bool any_bad = __any_sync(0xffffffffu, bad);
     const int units = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) {
-      // the cheapest of: S-way splits (S = 1, 2, 4, 8) and stream-K, costed as
-      // the longest CTA's K blocks plus kPieceCost per piece it runs;
-      // P = the most pieces one unit can be cut into
       int mode = 0, S = 1, P = 1;
-      const int grid = static_cast<int>(gridDim.x);
-      if (SWAP && args.counters && mx <= kSplitRows && units > 0 && units <= args.unit_cap) {
-        long long best = static_cast<long long>((units + grid - 1) / grid) * (kblocks + kPieceCost);
-        for (int c = 2; c <= kMaxSplit; c *= 2) {
-          if (kblocks % c || static_cast<long long>(units) * c > args.split_cap) continue;
-          const long long cost =
-              ((static_cast<long long>(units) * c + grid - 1) / grid) * (kblocks / c + kPieceCost);
-          if (cost < best) { best = cost; S = c; P = c; }
-        }
-        const long long tot = static_cast<long long>(units) * kblocks;
-        const long long share = tot / grid;
-        if (share >= 1) {
-          const int psk = static_cast<int>((kblocks + share - 1) / share) + 1;
-          const long long pieces_per_cta = (share + kblocks - 1) / kblocks + 1;
-          const long long cost = (tot + grid - 1) / grid + kPieceCost * pieces_per_cta;
-          if (cost < best && static_cast<long long>(units) * psk <= args.split_cap) {
-            best = cost; mode = 1; S = 1; P = psk;
-          }
-        }
-      }
+      if (SWAP && args.counters && mx <= kSplitRows && units > 0 && units <= args.unit_cap)
+        choose_split(units, kblocks, static_cast<int>(gridDim.x), args.split_cap, mode, S, P);
       s_split[0] = mode;
       s_split[6] = P;
       s_split[7] = S;
       *s_total = any_bad ? 0 : units;
-      *abort_flag = 0;
       if (any_bad && blockIdx.x == 0) set_status(args.status, MOE_ERR_DEVICE_CHECK);
     }
+    __syncwarp();
+  };
+  if (!deferred) {
+    // ---- group offsets into shared memory (all threads)
+    for (int i = threadIdx.x; i <= G; i += kThreads)
+      s_off[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows_max);
+    __syncthreads();
+    if (warp == 0) build_table();
+    __syncthreads();
+    // a CTA without work (or every CTA, when the offsets failed their check)
+    // leaves before it allocates tensor memory (with a leading phase, every CTA stays)
+    if (!pre && (*s_total == 0 || WorkIter(s_split[0], s_split[7], *s_total, kblocks, wgrid, wcta).empty())) return;
   }
-  __syncthreads();
-  const int units = *s_total;
-  const int mode = s_split[0];
-  const int P = s_split[6];
-  const int S = s_split[7];
-  // a CTA without work (or every CTA, when the offsets failed their check)
-  // leaves before it allocates tensor memory
-  if (units == 0 || WorkIter(mode, S, units, kblocks, wgrid, wcta).empty()) return;
+  // the routed phase's plan (read once the table is built) and the leading phase's (the same in every thread)
+  const int units = deferred ? 0 : *s_total;
+  const int mode = deferred ? 0 : s_split[0];
+  const int S = deferred ? 1 : s_split[7];
+  auto phase_r = [&]() { return Phase{s_split[0], s_split[7], s_split[6], *s_total, kblocks, false}; };
+  int pre_mode = 0, pre_S = 1, pre_P = 1;
+  const int pre_kblocks = pre ? args.pre_K / kBK : 0;
+  if (pre && args.pre_counters && args.pre_rows <= kSplitRows)
+    choose_split(args.pre_units, pre_kblocks, static_cast<int>(gridDim.x), args.pre_split_cap, pre_mode, pre_S,
+                 pre_P);
+  const Phase phase_s{pre_mode, pre_S, pre_P, pre ? args.pre_units : 0, pre_kblocks, true};
+  // (deferred) the unit table is there once table_bar flips
+  auto wait_table = [&]() { return mbar_wait(table_bar, 0, abort_flag, args.status, args.wait_ns); };
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
@@ -421,6 +469,18 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   };
 
   const int wrows = ACT == 1 ? 2 * args.N : args.N;   // weight rows per group
+  // the leading phase: one group of pre_rows rows from row 0, weight block = unit
+  auto decode_ph = [&](const Phase& ph, int idx, int& g, int& row0, int& nrows, int& wb, int& kind) {
+    if (ph.pre) {
+      g = 0;
+      row0 = 0;
+      nrows = args.pre_rows;
+      wb = idx;
+      kind = 0;
+      return;
+    }
+    decode(idx, g, row0, nrows, wb, kind);
+  };
 
   if (warp == 0 && WT) {
     // ------------------------------------------------------------ 8-bit weight producer
@@ -467,19 +527,25 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     long long issued = 0;
     int stage = 0;
     uint32_t phase = 0;
-    WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
+    auto produce = [&](const Phase& ph) -> bool {
+    WorkIter wi(ph.mode, ph.S, ph.units, ph.kblocks, wgrid, wcta);
     Piece pc;
+    // the leading phase: its own operand maps and weight rows, token rows straight from the map
+    const CUtensorMap* mt = ph.pre ? &tm_tok2 : &tm_tok;
+    const CUtensorMap* mw = ph.pre ? &tm_wgt2 : &tm_wgt;
+    const int nw = ph.pre ? args.pre_N : args.N;
+    const int32_t* a_rows = ph.pre ? nullptr : args.a_rows;
     while (wi.next(pc)) {
       int g, row0, nrows, wb, kind;
-      decode(pc.u, g, row0, nrows, wb, kind);
-      const int wrow = g * wrows + wb * C::kOutCols;
+      decode_ph(ph, pc.u, g, row0, nrows, wb, kind);
+      const int wrow = g * (ACT == 1 ? 2 * nw : nw) + wb * C::kOutCols;
       const int n16 = (nrows + 15) >> 4;
       // token rows fetched: SWAP 16-row multiples; tokens-on-M all 128 rows
       // (whole box) or, gathered, the live rows rounded up to 4
-      const int nfetch = SWAP ? n16 * 16 : (args.a_rows ? (nrows + 3) & ~3 : kBM_rows);
-      if (args.a_rows) {
+      const int nfetch = SWAP ? n16 * 16 : (a_rows ? (nrows + 3) & ~3 : kBM_rows);
+      if (a_rows) {
         __syncwarp();
-        for (int i = lane; i < nfetch; i += 32) s_gidx[i] = args.a_rows[row0 + min(i, nrows - 1)];
+        for (int i = lane; i < nfetch; i += 32) s_gidx[i] = a_rows[row0 + min(i, nrows - 1)];
         __syncwarp();
       }
       const uint32_t bytes = static_cast<uint32_t>(C::kABytes * (SWAP ? 1 : 0) + C::kBBytes * (SWAP ? 0 : 1) +
@@ -500,15 +566,15 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
               const int kq = kc + q * kBK;
               uint8_t* aq = sa + q * C::kABytes;
               uint8_t* bq = sb + q * (W * kBK * 2);
-              tma_load_2d(aq, &tm_wgt, &full_bar[stage], kq, wrow, pol_w);
-              if (ACT == 1) tma_load_2d(aq + kTileRows128, &tm_wgt, &full_bar[stage], kq, wrow + args.N, pol_w);
-              if (args.a_rows) {
+              tma_load_2d(aq, mw, &full_bar[stage], kq, wrow, pol_w);
+              if (ACT == 1) tma_load_2d(aq + kTileRows128, mw, &full_bar[stage], kq, wrow + nw, pol_w);
+              if (a_rows) {
                 for (int j = 0; j < nfetch; j += 4)
-                  tma_gather4(bq + j * kBK * 2, &tm_tok, &full_bar[stage], kq, s_gidx[j], s_gidx[j + 1],
+                  tma_gather4(bq + j * kBK * 2, mt, &full_bar[stage], kq, s_gidx[j], s_gidx[j + 1],
                               s_gidx[j + 2], s_gidx[j + 3], pol_tok);
               } else {
                 for (int j = 0; j < n16; ++j)
-                  tma_load_2d(bq + j * 16 * kBK * 2, &tm_tok, &full_bar[stage], kq, row0 + 16 * j, pol_tok);
+                  tma_load_2d(bq + j * 16 * kBK * 2, mt, &full_bar[stage], kq, row0 + 16 * j, pol_tok);
               }
             }
             ++issued;
@@ -537,7 +603,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
               tma_load_2d(sb, &tm_wgt, &full_bar[stage], kc, wrow, pol_w);
             }
           }
-          if (args.a_rows) {
+          if (a_rows) {
             for (int j = 0; j < nfetch; j += 4)
               tma_gather4(stok + j * kBK * 2, &tm_tok, &full_bar[stage], kc, s_gidx[j], s_gidx[j + 1],
                           s_gidx[j + 2], s_gidx[j + 3], pol_tok);
@@ -559,8 +625,18 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return false;
     }
+    return true;
+    };
+    bool run = !pre || produce(phase_s);
+    if (run && deferred) {
+      // the routed rows: wait for the previous kernel now, then build and publish the unit table
+      chain_wait();
+      build_table();
+      if (lane == 0) mbar_arrive(table_bar);
+    }
+    if (run) produce(phase_r());
     if (lane == 0) {
       // drain: every load issued into the ring has landed before the CTA may
       // exit (bounded wait that ignores `abort`; the normal path passes at once)
@@ -575,7 +651,8 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
+      auto mma = [&](const Phase& ph) -> bool {
+      WorkIter wi(ph.mode, ph.S, ph.units, ph.kblocks, wgrid, wcta);
       Piece pc;
       for (; wi.next(pc); ++it) {
         const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
@@ -584,7 +661,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         int chains = 1, cw = 0;
         if (SWAP) {
           int g, row0, nrows, wb, kind;
-          decode(pc.u, g, row0, nrows, wb, kind);
+          decode_ph(ph, pc.u, g, row0, nrows, wb, kind);
           const int n16 = (nrows + 15) >> 4;
           idesc = idesc_bf16_f32(128, n16 * 16);
           chains = swap_chains(n16, C::kAccCols, ACT == 1);
@@ -592,7 +669,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         } else {
           idesc = idesc_bf16_f32(128, W);
         }
-        if (!mbar_wait(&tempty_bar[ab], aphase ^ 1u, abort_flag, args.status, args.wait_ns)) break;
+        if (!mbar_wait(&tempty_bar[ab], aphase ^ 1u, abort_flag, args.status, args.wait_ns)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * C::kAccCols;
         // the accumulator chains' addresses (gate or plain chains, then up chains)
@@ -671,9 +748,12 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
             umma_commit(&empty_bar[stage]);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
+        if (!ok) return false;
         umma_commit(&tfull_bar[ab]);           // accumulator ab ready for the epilogue
       }
+      return true;
+      };
+      if ((!pre || mma(phase_s)) && (!deferred || wait_table())) mma(phase_r());
       // every MMA issued above has completed once done_bar flips
       umma_commit(done_bar);
       mbar_wait_timed(done_bar, 0, args.status);
@@ -683,14 +763,21 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     const int q = warp & 3;                    // TMEM lane quadrant of this warp
     const int lrow = q * 32 + lane;            // TMEM lane = accumulator row
     int it = 0;
-    WorkIter wi(mode, S, units, kblocks, wgrid, wcta);
+    auto epilogue = [&](const Phase& ph) -> bool {
+    WorkIter wi(ph.mode, ph.S, ph.units, ph.kblocks, wgrid, wcta);
     Piece pc;
+    const int P = ph.P;
+    // the leading phase writes its own output with its own split scratch
+    __nv_bfloat16* const out = ph.pre ? args.pre_out : args.out;
+    const int ldo = ph.pre ? args.pre_N : args.N;
+    int* const counters = ph.pre ? args.pre_counters : args.counters;
+    float* const partials = ph.pre ? args.pre_partials : args.partials;
     for (; wi.next(pc); ++it) {
       const int ab = C::kNumAcc == 2 ? (it & 1) : 0;
       const uint32_t aphase = (C::kNumAcc == 2 ? (it >> 1) : it) & 1;
       const int u = pc.u;
       int g, row0, nrows, wb, kind;
-      decode(u, g, row0, nrows, wb, kind);
+      decode_ph(ph, u, g, row0, nrows, wb, kind);
       // the warp leaves together or not at all (tcgen05.ld below is warp-wide)
       // (8-bit weights: the converter warps need the issue slots while this waits)
       bool ok = __all_sync(0xffffffffu, WT ? mbar_wait_sleep(&tfull_bar[ab], aphase, abort_flag, args.status,
@@ -702,7 +789,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         epi_bar_sync();
         ok = s_split[2] && s_split[3] && s_split[4] && s_split[5];
       }
-      if (!ok) break;
+      if (!ok) return false;
       tc_fence_after();
       const uint32_t t_acc = tmem_base + ab * C::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
       auto release_acc = [&]() {
@@ -713,7 +800,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
       if (SWAP) {
         // accumulator row = output column wb*128 + lrow; accumulator column =
         // token, chain c of gate (h = 0) / up (h = 1) at column (h*C + c)*cw
-        __nv_bfloat16* ocol = args.out + static_cast<size_t>(row0) * args.N + wb * 128 + lrow;
+        __nv_bfloat16* ocol = out + static_cast<size_t>(row0) * ldo + wb * 128 + lrow;
         // 8-bit weights: this accumulator row's scales (gate and up rows, or the row)
         float sg_scale = 1.f, su_scale = 1.f;
         if (WT) {
@@ -758,7 +845,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
             for (int i = 0; i < 16; ++i) {
               if (j * 16 + i < nrows) {
                 const float h = out_value(gs[i], us[i]);
-                ocol[static_cast<size_t>(j * 16 + i) * args.N] = __float2bfloat16_rn(h);
+                ocol[static_cast<size_t>(j * 16 + i) * ldo] = __float2bfloat16_rn(h);
               }
             }
           }
@@ -771,7 +858,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
           load_chunk(0, gm, um);
           release_acc();
           float4* mine = reinterpret_cast<float4*>(
-              args.partials + ((static_cast<size_t>(u) * P + pc.pi) * 128 + lrow) * PF);
+              partials + ((static_cast<size_t>(u) * P + pc.pi) * 128 + lrow) * PF);
           const int n4 = (nrows + 3) >> 2;   // float4s per half that hold live tokens
 #pragma unroll
           for (int i = 0; i < kSplitRows / 4; ++i) {
@@ -783,11 +870,11 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
           __threadfence();
           epi_bar_sync();
           if (threadIdx.x == 64) {
-            const int old = atomicAdd(&args.counters[u], 1);
+            const int old = atomicAdd(&counters[u], 1);
             int last = 0;
             if (old == pc.np - 1) {
               last = 1;
-              atomicExch(&args.counters[u], 0);   // every ticket of this unit is taken: back to zero
+              atomicExch(&counters[u], 0);   // every ticket of this unit is taken: back to zero
             } else if (old < 0 || old >= pc.np) {
               set_status(args.status, MOE_ERR_DEVICE_CHECK);   // counters were not zero at entry
             }
@@ -800,7 +887,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kSplitRows; ++i) { gs[i] = 0.f; us[i] = 0.f; }
             const float4* slot0 = reinterpret_cast<const float4*>(
-                args.partials + (static_cast<size_t>(u) * P * 128 + lrow) * PF);
+                partials + (static_cast<size_t>(u) * P * 128 + lrow) * PF);
             const size_t slot_f4 = static_cast<size_t>(128) * PF / 4;   // float4s per piece slot
 #pragma unroll
             for (int i = 0; i < kSplitRows / 4; ++i) {
@@ -825,7 +912,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
             for (int i = 0; i < kSplitRows; ++i) {
               if (i < nrows) {
                 const float h = out_value(gs[i], us[i]);
-                ocol[static_cast<size_t>(i) * args.N] = __float2bfloat16_rn(h);
+                ocol[static_cast<size_t>(i) * ldo] = __float2bfloat16_rn(h);
               }
             }
           }
@@ -890,6 +977,9 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
         release_acc();
       }
     }
+    return true;
+    };
+    if ((!pre || epilogue(phase_s)) && (!deferred || wait_table())) epilogue(phase_r());
   } else if (WT && warp == 6 + kConvWarps) {
     // ------------------------------------------------------------ token producer
     // lane 0 loads the token tile of each K block (the unit's rows: 16-row
@@ -1113,7 +1203,7 @@ template <int SWAP, int W, int ACT, int MC = 0, int WT = 0>
 int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K, void* out,
                int* status, const GemmScratch* scratch, int grid_cap, cudaStream_t stream, int* launches,
                int max_slots = kMaxSlots, int K_a = 0, const int32_t* a_rows = nullptr, int a_src_rows = 0,
-               const float* w_scale = nullptr) {
+               const float* w_scale = nullptr, const LeadPhase* lead = nullptr) {
   using C = Cfg<SWAP, W, ACT, MC, WT>;
   constexpr int kThreads = C::kThreads;
   auto kernel = grouped_gemm_kernel<SWAP, W, ACT, MC, WT>;
@@ -1167,7 +1257,30 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
   long long bound = (static_cast<long long>((rows_max + C::kUnitRows - 1) / C::kUnitRows) + nonempty) *
                     (N / C::kOutCols / (MC ? 2 : 1));
   GemmArgs args{offsets, G, rows_max, N, K, reinterpret_cast<__nv_bfloat16*>(out), status, SWAP ? 1 : 0,
-                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows, wait_limit_ns(), w_scale};
+                nullptr, nullptr, 0, 0, K_a ? K_a / kBK : 0, a_rows, wait_limit_ns(), w_scale,
+                0, 0, 0, 0, 0, nullptr, nullptr, nullptr, 0};
+  // the leading phase's operand maps (without one, the launch's own maps stand in)
+  CUtensorMap tt2 = tt, tw2 = tw;
+  if (lead) {
+    if (!SWAP || WT || !lead_phase_applies(lead->rows, lead->N, lead->K)) return MOE_ERR_UNSUPPORTED;
+    const int lrows = ACT == 1 ? 2 * lead->N : lead->N;
+    if (!make_map(&tt2, lead->a, static_cast<uint64_t>(lead->rows), static_cast<uint64_t>(lead->K), 16) ||
+        !make_map(&tw2, lead->w, static_cast<uint64_t>(lrows), static_cast<uint64_t>(lead->K), 128))
+      return MOE_ERR_CUDA;
+    args.pre_units = lead->N / 128;
+    args.pre_N = lead->N;
+    args.pre_K = lead->K;
+    args.pre_rows = lead->rows;
+    args.pre_early = lead->early ? 1 : 0;
+    args.pre_out = static_cast<__nv_bfloat16*>(lead->out);
+    const SplitPlan lp = split_plan(1, lead->rows, lead->N, ACT, max_slots);
+    if (lead->scratch.counters && lead->scratch.partials && lp.partial_bytes &&
+        lead->scratch.partial_bytes >= lp.partial_bytes && args.pre_units <= lp.unit_cap) {
+      args.pre_counters = lead->scratch.counters;
+      args.pre_partials = static_cast<float*>(lead->scratch.partials);
+      args.pre_split_cap = lp.split_cap;
+    }
+  }
   if (SWAP && scratch && scratch->counters && scratch->partials) {
     const SplitPlan p = split_plan(G, rows_max, N, ACT, max_slots);
     if (p.partial_bytes && scratch->partial_bytes >= p.partial_bytes) {
@@ -1185,14 +1298,16 @@ int launch_cfg(const void* a, const void* w, const int32_t* offsets, int G, int 
     if (pairs > bound) pairs = bound;
     if (pairs < 1) pairs = 1;
     if (launch_chained_cluster(kernel, dim3(static_cast<int>(2 * pairs)), dim3(kThreads), C::kSmemBytes, stream, 2,
-                               tt, tw, args) != cudaSuccess)
+                               tt, tw, tt2, tw2, args) != cudaSuccess)
       return MOE_ERR_CUDA;
     ++*launches;
     return MOE_OK;
   }
-  int grid = static_cast<int>(bound < grid_cap ? bound : grid_cap);
+  // (a leading phase spreads over every CTA the launch may have)
+  int grid = static_cast<int>(bound < grid_cap && !lead ? bound : grid_cap);
   if (grid < 1) grid = 1;
-  if (launch_chained(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, tt, tw, args) != cudaSuccess)
+  if (launch_chained(kernel, dim3(grid), dim3(kThreads), C::kSmemBytes, stream, tt, tw, tt2, tw2, args) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   ++*launches;
   return MOE_OK;
@@ -1206,6 +1321,10 @@ constexpr bool kPairs = true;
 
 bool grouped_gemm_weights_on_m(int G, int rows_max, int N) {
   return N % 128 == 0 && static_cast<long long>(rows_max) <= 64LL * G;
+}
+
+bool lead_phase_applies(int rows, int N, int K) {
+  return rows >= 1 && rows <= kSplitRows && N % 128 == 0 && K % kBK == 0 && K > 0;
 }
 
 size_t grouped_gemm_counter_region_bytes() { return static_cast<size_t>(kCounterInts) * sizeof(int); }
@@ -1237,12 +1356,13 @@ GemmScratch grouped_gemm_scratch(void* ws, size_t ws_bytes) {
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, const GemmScratch* scratch, int grid_cap, cudaStream_t stream,
                         int* launches, const int32_t* a_rows, int a_src_rows, int max_slots, int max_group_rows,
-                        const float* w_scale) {
+                        const float* w_scale, const LeadPhase* lead) {
   if (rows_max == 0) return MOE_OK;
   if (max_slots <= 0) max_slots = kMaxSlots;
   // groups of one row: a weight stream on the CUDA cores
   const int bound = rows_max == 1 ? 1 : max_group_rows;
-  if (act != 2 && grouped_gemv_applies(G, N, K, act, bound))
+  if (lead && (w_scale || act == 2)) return MOE_ERR_UNSUPPORTED;
+  if (!lead && act != 2 && grouped_gemv_applies(G, N, K, act, bound))
     return grouped_gemv_launch(a, w, w_scale, offsets, G, rows_max, N, K, act, out, status, stream, launches, a_rows,
                                a_src_rows, bound, grid_cap);
   if (w_scale) {
@@ -1257,10 +1377,11 @@ int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, in
   if (grouped_gemm_weights_on_m(G, rows_max, N)) {
     if (act == 1)
       return launch_cfg<1, kSwapRows, 1>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,
-                                         launches, max_slots, 0, a_rows, a_src_rows);
+                                         launches, max_slots, 0, a_rows, a_src_rows, nullptr, lead);
     return launch_cfg<1, kSwapRows, 0>(a, w, offsets, G, rows_max, N, K, out, status, scratch, grid_cap, stream,
-                                       launches, max_slots, 0, a_rows, a_src_rows);
+                                       launches, max_slots, 0, a_rows, a_src_rows, nullptr, lead);
   }
+  if (lead) return MOE_ERR_UNSUPPORTED;   // (a leading phase joins weights-on-M launches of bf16 weights only)
   // the pairs multicast operand tiles inside a cluster of this GPU: only for
   // operands in this GPU's own device memory
   const bool pairs_ok = kPairs && !a_rows && grid_cap >= 2 && (N % 256 == 0 || N % 512 == 0);

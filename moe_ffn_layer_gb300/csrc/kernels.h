@@ -56,10 +56,26 @@ GemmScratch grouped_gemm_scratch(void* ws, size_t ws_bytes);
 // max_group_rows (0: unknown): a bound on any group's rows that the caller knows.
 // w_scale (nullable): w holds e4m3 codes with one fp32 scale per weight row
 // (weights-on-M shapes and one-row groups only; others MOE_ERR_UNSUPPORTED).
+// A leading phase of a weights-on-M launch (bf16 weights): one group of
+// rows <= 16 token rows a [rows][K] times weights w ([2N][K] with SiLU*mul,
+// else [N][K]) into out [rows][N], with split-K scratch of its own; early:
+// it runs before the launch waits on the previous kernel of the stream, so a
+// and w must not come from that kernel.
+struct LeadPhase {
+  const void* a;
+  const void* w;
+  int rows, N, K;
+  void* out;
+  bool early;
+  GemmScratch scratch;
+};
+// Whether a leading phase of these sizes can join a launch (rows, N and K as above).
+bool lead_phase_applies(int rows, int N, int K);
 int grouped_gemm_launch(const void* a, const void* w, const int32_t* offsets, int G, int rows_max, int N, int K,
                         int act, void* out, int* status, const GemmScratch* scratch, int grid_cap,
                         cudaStream_t stream, int* launches, const int32_t* a_rows = nullptr, int a_src_rows = 0,
-                        int max_slots = 0, int max_group_rows = 0, const float* w_scale = nullptr);
+                        int max_slots = 0, int max_group_rows = 0, const float* w_scale = nullptr,
+                        const LeadPhase* lead = nullptr);
 int grouped_gemm_max_groups();
 // Groups of one row (max_group_rows: a bound the caller knows, e.g. T when a
 // token adds at most one row per group) run on the CUDA cores: a weight stream

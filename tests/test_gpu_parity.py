@@ -693,6 +693,36 @@ def test_operands_outside_device_memory_are_refused():
     no_device_error()
 
 
+@pytest.mark.parametrize("T", [4, 9])
+def test_forward_shared_expert_as_leading_phase(T):
+    """4 to 9 tokens: the shared expert leads the routed matmul launches (its
+    gate_up before the gate_up launch waits on the router), no side stream:
+    four launches, the oracle's output, the same bits on a second call and
+    through a CUDA graph."""
+    L = layer("tiny", T)
+    x = x_tensor("tiny", T)
+    ref = om.forward(inputs("tiny", T), synth.workload("tiny", T).k)
+    a = L.forward(x).clone()
+    assert B.moe_last_launch_count() == 4   # router with dispatch, gate_up, down, combine
+    no_device_error()
+    assert_close_layer(to_f64(a), ref["out"], f"tiny T={T}")
+    b = L.forward(x).clone()
+    g_out = torch.empty_like(a)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        L.forward(x, g_out, s)   # (sizes the workspace on this stream before capture)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        L.forward(x, g_out, torch.cuda.current_stream())
+    g_out.fill_(0)
+    g.replay()
+    torch.cuda.synchronize()
+    no_device_error()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), g_out.view(torch.int16))
+
+
 def test_forward_repeatable_and_launch_count():
     """Two calls give identical bits; the launch count is what the call reports."""
     L = layer("tiny", 16)
