@@ -46,7 +46,8 @@
 // weight block, row block) so that CTAs running side by side share a weight
 // block in L2.
 //
-// Stream-K (weights-on-M form, every group <= 16 rows, scratch given): when
+// Stream-K (weights-on-M form, every group <= 16 rows, scratch given; gate_up
+// and 8-bit launches): when
 // whole units do not spread evenly over the grid, the units' K blocks are laid
 // end to end and every CTA takes an equal contiguous share.  A unit cut
 // between CTAs becomes pieces; each piece stores its fp32 partial accumulator
@@ -253,10 +254,11 @@ struct WorkIter {
 constexpr int kPieceCost = 6;
 
 // Split plan of a phase whose groups all hold <= kSplitRows rows: the cheapest
-// of S-way splits (S = 1, 2, 4, 8) and stream-K, costed as the longest CTA's K
-// blocks plus kPieceCost per piece it runs; P = the most pieces one unit can
-// be cut into.
-__device__ void choose_split(int units, int kblocks, int grid, long long split_cap, int& mode, int& S, int& P) {
+// of S-way splits (S = 1, 2, 4, 8) and (streamk) stream-K, costed as the
+// longest CTA's K blocks plus kPieceCost per piece it runs; P = the most
+// pieces one unit can be cut into.
+__device__ void choose_split(int units, int kblocks, int grid, long long split_cap, bool streamk, int& mode, int& S,
+                             int& P) {
   mode = 0;
   S = 1;
   P = 1;
@@ -268,7 +270,7 @@ __device__ void choose_split(int units, int kblocks, int grid, long long split_c
   }
   const long long tot = static_cast<long long>(units) * kblocks;
   const long long share = tot / grid;
-  if (share >= 1) {
+  if (streamk && share >= 1) {
     const int psk = static_cast<int>((kblocks + share - 1) / share) + 1;
     const long long pieces_per_cta = (share + kblocks - 1) / kblocks + 1;
     const long long cost = (tot + grid - 1) / grid + kPieceCost * pieces_per_cta;
@@ -317,6 +319,11 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = args.G;
   const int NB = args.N / C::kOutCols;   // weight blocks per group
+  // stream-K for gate_up launches (and the 8-bit form) only: at decode sizes the
+  // bf16 down's units are short (K = I), and the partial sums that end every
+  // CTA's range cost more than the balance gains (measured: decode T=6
+  // 96.5 -> 92.8 us, T=14 144.1 -> 142.2 us, no size slower)
+  constexpr bool kStreamK = ACT == 1 || WT;
 
   // ---- prologue (may overlap the previous kernel of the stream): barriers,
   // tensor-map prefetch; then wait for that kernel's writes
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
     if (lane == 0) {
       int mode = 0, S = 1, P = 1;
       if (SWAP && args.counters && mx <= kSplitRows && units > 0 && units <= args.unit_cap)
-        choose_split(units, kblocks, static_cast<int>(gridDim.x), args.split_cap, mode, S, P);
+        choose_split(units, kblocks, static_cast<int>(gridDim.x), args.split_cap, kStreamK, mode, S, P);
       s_split[0] = mode;
       s_split[6] = P;
       s_split[7] = S;
@@ -420,8 +427,8 @@ __global__ void __launch_bounds__(Cfg<SWAP, W, ACT, MC, WT>::kThreads, 1)
   int pre_mode = 0, pre_S = 1, pre_P = 1;
   const int pre_kblocks = pre ? args.pre_K / kBK : 0;
   if (pre && args.pre_counters && args.pre_rows <= kSplitRows)
-    choose_split(args.pre_units, pre_kblocks, static_cast<int>(gridDim.x), args.pre_split_cap, pre_mode, pre_S,
-                 pre_P);
+    choose_split(args.pre_units, pre_kblocks, static_cast<int>(gridDim.x), args.pre_split_cap, kStreamK, pre_mode,
+                 pre_S, pre_P);
   const Phase phase_s{pre_mode, pre_S, pre_P, pre ? args.pre_units : 0, pre_kblocks, true};
   // (deferred) the unit table is there once table_bar flips
   auto wait_table = [&]() { return mbar_wait(table_bar, 0, abort_flag, args.status, args.wait_ns); };
