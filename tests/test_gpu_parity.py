@@ -644,6 +644,49 @@ def test_forward_dispatch_bit_exact(name, T):
     ws.fill_(0)        # leave the workspace as the layer expects it (counters zero)
 
 
+def _random_layer(seed: int):
+    """A seeded layer shape within the supported ranges (H, I, I_s multiples
+    of 64; k <= min(E, 16)), with or without router bias and shared expert."""
+    r = np.random.default_rng(1000 + seed)
+    E = int(r.choice([2, 4, 8, 16, 32, 64, 256]))
+    k = int(r.integers(1, min(E, 16) + 1)) if r.random() < 0.3 else int(r.integers(1, min(E, 8) + 1))
+    wl = synth.Workload(f"random{seed}", int(r.choice([1, 2, 3, 5, 7, 9, 13, 16, 17, 33, 64, 100, 257, 600])),
+                        int(r.choice([128, 256, 384, 512, 1024])), E, k, int(r.choice([64, 128, 192, 256, 512])),
+                        int(r.choice([0, 64, 128, 256])), sigma_router=0.1, sigma_w=0.03,
+                        zipf_s=1.1 if r.random() < 0.4 else None)
+    return wl
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_forward_random_shapes(seed):
+    """Seeded random layer shapes (batch size, hidden and expert sizes, experts,
+    top-k, shared expert or none, skewed routing or not): the layer output
+    within the layer tolerance of the oracle, and the dispatch the forward
+    computed (read from its workspace) bit-exact."""
+    wl = _random_layer(seed)
+    T = wl.T
+    inp = synth.make_inputs(wl, seed)
+    ref = om.forward(inp, wl.k)
+    ids_ref, w_ref, _ = om.route(inp["x"], inp["w_router"], inp["bias"], wl.k)
+    off_ref, st_ref, inv_ref = om.permute(ids_ref, wl.E)
+    L = MoEFFN.from_inputs(inp, wl.k, "cuda")
+    ws = L.workspace(T)
+    out = L.forward(bf16_tensor(inp["x"], "cuda")).clone()
+    no_device_error()
+    shape = f"T={T} H={wl.H} E={wl.E} k={wl.k} I={wl.I} I_s={wl.Is} zipf={wl.zipf_s}"
+    assert_close_layer(to_f64(out), ref["out"], shape)
+    o = B.moe_workspace_layout(L.dims, T)
+    Tk = T * wl.k
+
+    def region(off, n, dtype):
+        return ws[off:off + n * 4].view(dtype).cpu().numpy()
+
+    np.testing.assert_array_equal(region(o.topk_ids, Tk, torch.int32).reshape(T, wl.k), ids_ref, err_msg=shape)
+    np.testing.assert_array_equal(region(o.expert_offsets, wl.E + 1, torch.int32), off_ref, err_msg=shape)
+    np.testing.assert_array_equal(region(o.sorted_token, Tk, torch.int32), st_ref, err_msg=shape)
+    np.testing.assert_array_equal(region(o.inv_perm, Tk, torch.int32), inv_ref, err_msg=shape)
+
+
 @pytest.mark.parametrize("name,T", [("decode", 1), ("decode", 8), ("batched_decode", 256), ("prefill", 8192)])
 def test_forward_graph_replay_matches_eager(name, T):
     """The forward captured in a CUDA graph (as the benchmark times it) and

@@ -194,6 +194,27 @@ def test_forward_w8(name, T):
     assert torch.equal(out.view(torch.int16), o.view(torch.int16))
 
 
+@pytest.mark.parametrize("seed", range(16))
+def test_forward_w8_random_shapes(seed):
+    """Seeded random layer shapes with e4m3 routed weights, within the sizes the
+    8-bit path takes (I and H multiples of 128, T*k <= 64 E): every output
+    element against the oracle on the same codes and scales."""
+    r = np.random.default_rng(2000 + seed)
+    E = int(r.choice([4, 8, 16, 64, 128]))
+    k = int(r.integers(1, min(E, 8) + 1))
+    T = int(r.choice([t for t in (1, 2, 3, 5, 8, 13, 16, 24, 64, 200) if t * k <= 64 * E]))
+    wl = synth.Workload(f"w8random{seed}", T, int(r.choice([128, 256, 512, 1024])), E, k,
+                        int(r.choice([128, 256, 512])), int(r.choice([0, 128, 256])), sigma_router=0.1,
+                        sigma_w=0.03, zipf_s=1.1 if r.random() < 0.4 else None)
+    inp = synth.make_inputs_w8(wl, seed)
+    ref = om.forward(inp, k)
+    L = MoEFFN.from_inputs(inp, k, "cuda")
+    out = L.forward(bf16_tensor(inp["x"], "cuda")).clone()
+    no_device_error()
+    assert_close_layer(to_f64(out), ref["out"],
+                       f"w8 T={T} H={wl.H} E={E} k={k} I={wl.I} I_s={wl.Is} zipf={wl.zipf_s}")
+
+
 def test_forward_w8_refuses_prefill_sizes():
     base = _w8_layer("decode")
     x = torch.zeros((8192, 2048), dtype=torch.bfloat16, device="cuda")
