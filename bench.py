@@ -57,6 +57,7 @@ SWEEP = [("decode", 1), ("decode", 4), ("decode", 8), ("batched_decode", 64), ("
          ("decode_w8", 1), ("decode_w8", 4), ("decode_w8", 8), ("batched_decode_w8", 64),
          ("batched_decode_w8", 256)]
 SWEEP_SECONDS = 0.25          # timed replays per sweep workload
+MIN_FORWARDS_PER_GRAPH = 8    # a model's decode step holds dozens of MoE layers in one graph
 ONE_GPU = ("one GPU only: the layer does not shard, and its prefill matmuls share operand tiles between the two "
            "CTAs of a cluster by TMA multicast, which stays inside one GPU's own memory")
 
@@ -136,7 +137,8 @@ def config_of(w) -> dict:
             "weights": ("routed experts e4m3 with per-row fp32 scales, shared expert bf16" if is_w8(w)
                         else "bf16"),
             "l2": f"expert weights rotate over {R} device copies ({R} x {touched / 1e6:.0f} MB touched >= 4 x L2); "
-                  f"one CUDA graph per copy, replayed back to back"}
+                  f"the timed CUDA graph holds consecutive forwards over the copies in turn (as consecutive MoE "
+                  f"layers of a model run in one graph), replayed back to back"}
 
 
 # ---------------------------------------------------------------- clocks
@@ -331,12 +333,36 @@ def measure(w, bed, args, clk, K, W, headline=False):
         if K is None:                           # sweep: about SWEEP_SECONDS of replays
             ms, _, _ = _timed_graph(graphs, stream, 2 * R, e0, e1)
             K = int(min(20000, max(20, SWEEP_SECONDS * 1e3 / max(ms / (2 * R), 1e-3))))
+            K = -(-K // max(R, MIN_FORWARDS_PER_GRAPH)) * max(R, MIN_FORWARDS_PER_GRAPH)
         torch.cuda.synchronize()
-        ms, t0, t1 = _timed_graph(graphs, stream, K, e0, e1, pre_s=0.15 if headline else 0.0,
+        # one forward per graph, replayed back to back: every forward also pays
+        # the gap between two graph launches (reported beside the value)
+        ms1, _, _ = _timed_graph(graphs, stream, K, e0, e1)
+    torch.cuda.synchronize()
+    # The timed graph holds F consecutive forwards, forward j on weight copy
+    # j mod R, as consecutive MoE layers of a model's decode step run inside
+    # one graph; F is the smallest divisor of K not below R or
+    # MIN_FORWARDS_PER_GRAPH (else K), so that the K timed steps are whole
+    # replays.
+    F = next((f for f in range(max(R, MIN_FORWARDS_PER_GRAPH), K + 1) if K % f == 0), K)
+    gm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gm, stream=stream):
+        cs = torch.cuda.current_stream()
+        for j in range(F):
+            layers[j % R].forward(x, outs[j % R], cs)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(-(-W // F)):
+            gm.replay()
+        stream.synchronize()
+        ms, t0, t1 = _timed_graph([gm], stream, K // F, e0, e1, pre_s=0.15 if headline else 0.0,
                                   post_s=0.1 if headline else 0.0)
     torch.cuda.synchronize()
     clocks = clk.window(t0, t1, pad=0.03)
     assert B.moe_last_device_error(stream) == 0
+    # every copy holds the same weights: each output of the timed graph equals the eager one
+    graph_same = graph_same and all(torch.equal(o.view(torch.int16), eager0.view(torch.int16))
+                                    for o in outs[:min(R, F)])
     value = tokens_per_s(w.T, K, ms)
 
     # the routing of this batch, through the route and permute calls
@@ -365,6 +391,7 @@ def measure(w, bed, args, clk, K, W, headline=False):
                   "peaks": f"{pk_src}: {pk['hbm_gbs']} GB/s, {pk['bf16_tflops_sustained']} TFLOP/s sustained"}
     roof = dominant_kernel(w, copies, wr, b, x, offs, xperm, nonempty, pk, pk_src, stream, e0, e1, K)
     res = {"value": value, "ms_per_step": ms / K, "steps": K, "warmup": W, "layer_roofline": layer_roof,
+           "forwards_per_graph": F, "ms_per_step_one_forward_per_graph": ms1 / K,
            "roofline": roof, "clocks": clocks, "launches_per_step": launches, "graph_matches_eager": graph_same,
            "config": config_of(w)}
     if headline:
@@ -507,7 +534,9 @@ def run_gpu(args, w):
             for name, T in SWEEP:
                 wl = synth.workload(name, T)
                 r = measure(wl, bed_for(wl), args, clk, None, 5)
-                sweep[r["config"]["workload"]] = {k: r[k] for k in ("value", "ms_per_step", "steps", "layer_roofline",
+                sweep[r["config"]["workload"]] = {k: r[k] for k in ("value", "ms_per_step", "steps", "forwards_per_graph",
+                                                                    "ms_per_step_one_forward_per_graph",
+                                                                    "layer_roofline",
                                                                     "roofline", "clocks", "launches_per_step",
                                                                     "graph_matches_eager")}
     finally:
@@ -521,6 +550,8 @@ def run_gpu(args, w):
         "gpu_launches": args.steps * head["launches_per_step"], "launches_per_step": head["launches_per_step"],
         "roofline": head["roofline"], "layer_roofline": head["layer_roofline"], "cpu_baseline": cpu,
         "graph_matches_eager": head["graph_matches_eager"],
+        "forwards_per_graph": head["forwards_per_graph"],
+        "ms_per_step_one_forward_per_graph": head["ms_per_step_one_forward_per_graph"],
         "clocks_note": "sampled every 20 ms; the headline window spans 0.15 s of untimed replays of the same "
                        "graphs before the timed steps and 0.1 s after them",
     }
