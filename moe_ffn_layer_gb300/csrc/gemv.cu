@@ -57,12 +57,13 @@ struct WeightChunk<1> {
   static constexpr int kBytes = 1;
 };
 
-// The non-empty groups in ascending order into s_groups, their number into
-// *s_count (every thread of the CTA takes part; one round of offset loads).  A
-// group with more rows than max_rows, or offsets out of range, is a device-side
-// error: recorded, skipped.  Without offsets the one group holds rows_max rows.
+// The non-empty groups in ascending order into s_groups, their first rows and
+// row counts into s_r0 / s_nr, their number into *s_count (every thread of the
+// CTA takes part; one round of offset loads).  A group with more rows than
+// max_rows, or offsets out of range, is a device-side error: recorded,
+// skipped.  Without offsets the one group holds rows_max rows.
 __device__ __forceinline__ void list_groups(const int32_t* __restrict__ offsets, int G, int rows_max, int max_rows,
-                                            int* status, int* s_groups, int* s_count) {
+                                            int* status, int* s_groups, int* s_r0, int* s_nr, int* s_count) {
   constexpr int kChunks = kMaxGemvGroups / kGemvThreads;
   constexpr int kWarps = kGemvThreads / 32;
   static_assert(kChunks * kWarps == 32, "one warp scans the (chunk, warp) counts");
@@ -107,8 +108,12 @@ __device__ __forceinline__ void list_groups(const int32_t* __restrict__ offsets,
   __syncthreads();
 #pragma unroll
   for (int c = 0; c < kChunks; ++c)
-    if (mask[c] >> lane & 1u)
-      s_groups[s_base[c * kWarps + warp] + __popc(mask[c] & ((1u << lane) - 1u))] = c * kGemvThreads + threadIdx.x;
+    if (mask[c] >> lane & 1u) {
+      const int slot = s_base[c * kWarps + warp] + __popc(mask[c] & ((1u << lane) - 1u));
+      s_groups[slot] = c * kGemvThreads + threadIdx.x;
+      s_r0[slot] = lo[c];
+      s_nr[slot] = hi[c] - lo[c];
+    }
   __syncthreads();
 }
 
@@ -119,11 +124,13 @@ __device__ __forceinline__ void list_groups(const int32_t* __restrict__ offsets,
 // scale per weight row ([G][2N] or [G][N]), applied to each dot product.
 // One warp, one item: output block n0 (one column with SiLU*mul, kRowsDown
 // without) of group g, whose token rows are r0 .. r0 + nr - 1.
+// src (optional): the R source rows of `a` for the group's token rows, already
+// resolved (then a_rows is not read).
 template <int ACT, int R, int WT>
 __device__ __forceinline__ void gemv_item(const __nv_bfloat16* __restrict__ a, const uint8_t* __restrict__ w,
                                           const float* __restrict__ wscale, int g, int n0, int r0, int nr, int N,
                                           int K, const int32_t* __restrict__ a_rows, int a_src_rows, int rows_max,
-                                          __nv_bfloat16* __restrict__ out) {
+                                          __nv_bfloat16* __restrict__ out, const int* src_rows = nullptr) {
   using WC = WeightChunk<WT>;
   constexpr int NW = ACT == 1 ? 2 : kRowsDown;   // weight rows per warp
   constexpr int NPW = ACT == 1 ? 1 : kRowsDown;  // output columns per warp
@@ -140,9 +147,14 @@ __device__ __forceinline__ void gemv_item(const __nv_bfloat16* __restrict__ a, c
   const __nv_bfloat16* ar[R];
 #pragma unroll
   for (int j = 0; j < R; ++j) {
-    const int r = r0 + (j < nr ? j : nr - 1);
-    int src = a_rows ? a_rows[r] : r;
-    if (src < 0 || src >= (a_rows ? a_src_rows : rows_max)) src = 0;   // checked upstream; never out of range
+    int src;
+    if (src_rows) {
+      src = src_rows[j];
+    } else {
+      const int r = r0 + (j < nr ? j : nr - 1);
+      src = a_rows ? a_rows[r] : r;
+      if (src < 0 || src >= (a_rows ? a_src_rows : rows_max)) src = 0;   // checked upstream; never out of range
+    }
     ar[j] = a + static_cast<size_t>(src) * K;
   }
   float acc[NW][R];
@@ -232,6 +244,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
                         __nv_bfloat16* __restrict__ out, int* status, const GemvPre pre) {
   constexpr int NPW = ACT == 1 ? 1 : kRowsDown;  // output columns per warp
   __shared__ int s_groups[kMaxGemvGroups];
+  __shared__ int s_r0[kMaxGemvGroups], s_nr[kMaxGemvGroups];
+  __shared__ int s_src[kMaxGemvGroups * R];      // source rows of a listed group's token rows
   __shared__ int s_count;
   const int warp = threadIdx.x >> 5;
   const long long wstride = static_cast<long long>(gridDim.x) * (kGemvThreads / 32);
@@ -241,15 +255,24 @@ __global__ void __launch_bounds__(kGemvThreads, 2)
       gemv_item<1, 1, 0>(pre.a, pre.w, nullptr, 0, static_cast<int>(item), 0, 1, pre.N, K, nullptr, 0, 1, pre.out);
   chain_wait();
   const ChainReleaseAtExit release_next;
-  list_groups(offsets, G, rows_max, R, status, s_groups, &s_count);
+  list_groups(offsets, G, rows_max, R, status, s_groups, s_r0, s_nr, &s_count);
+  // every listed group's source rows, resolved once (one round of loads), so
+  // that an item's first memory access is its weight stream
+  for (int i = threadIdx.x; i < s_count * R; i += kGemvThreads) {
+    const int sl = i / R, j = i - sl * R;
+    const int r = s_r0[sl] + (j < s_nr[sl] ? j : s_nr[sl] - 1);
+    int src = a_rows ? a_rows[r] : r;
+    if (src < 0 || src >= (a_rows ? a_src_rows : rows_max)) src = 0;   // checked upstream; never out of range
+    s_src[i] = src;
+  }
+  __syncthreads();
   const int blocks = N / NPW;                     // output blocks per group
   const long long items = static_cast<long long>(s_count) * blocks;
   for (long long item = wfirst; item < items; item += wstride) {
-    const int g = s_groups[item / blocks];
+    const int sl = static_cast<int>(item / blocks);
     const int n0 = static_cast<int>(item % blocks) * NPW;
-    const int r0 = offsets ? offsets[g] : 0;
-    const int nr = (offsets ? offsets[g + 1] : rows_max) - r0;
-    gemv_item<ACT, R, WT>(a, w, wscale, g, n0, r0, nr, N, K, a_rows, a_src_rows, rows_max, out);
+    gemv_item<ACT, R, WT>(a, w, wscale, s_groups[sl], n0, s_r0[sl], s_nr[sl], N, K, a_rows, a_src_rows, rows_max,
+                          out, s_src + sl * R);
   }
 }
 
@@ -283,11 +306,15 @@ __global__ void __launch_bounds__(kGemvThreads)
   __shared__ float s_y[kTailSlots][kTailCols];   // y_j[n], bf16-rounded
   __shared__ int s_live[kTailSlots];
   __shared__ float s_sh[kTailCols];              // the shared expert's down, column n0 + j from warp j
+  __shared__ float s_w[kTailSlots];              // the slots' combine weights
   static_assert(kTailCols == kTailSlots, "one warp per column of the shared expert's down");
   using WC = WeightChunk<WT>;
   chain_wait();
   const ChainReleaseAtExit release_next;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // this warp's slot row and weight, loaded beside the offsets (one round)
+  const int r_slot = warp < k ? __ldg(inv_perm + warp) : -1;
+  const float w_slot = threadIdx.x < k ? __ldg(topk_w + threadIdx.x) : 0.f;
   if (threadIdx.x < kTailSlots) s_group[threadIdx.x] = -1;
   __syncthreads();
   for (int g = threadIdx.x; g < G; g += kGemvThreads) {
@@ -300,7 +327,7 @@ __global__ void __launch_bounds__(kGemvThreads)
   const int n0 = blockIdx.x * kTailCols;
   const int j = warp;
   if (j < k) {
-    const int r = __ldg(inv_perm + j);
+    const int r = r_slot;
     const int g = (r >= 0 && r < rows) ? s_group[r] : -1;   // a row no group holds adds nothing
     float acc[kTailCols];
 #pragma unroll
@@ -379,12 +406,13 @@ __global__ void __launch_bounds__(kGemvThreads)
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) s_sh[warp] = acc;
   }
+  if (threadIdx.x < kTailSlots) s_w[threadIdx.x] = w_slot;
   __syncthreads();
   if (threadIdx.x < kTailCols && n0 + static_cast<int>(threadIdx.x) < N) {
     const int n = n0 + threadIdx.x;
     float v = 0.f;
     for (int s = 0; s < k; ++s)
-      if (s_live[s]) v = fmaf(__ldg(topk_w + s), s_y[s][threadIdx.x], v);
+      if (s_live[s]) v = fmaf(s_w[s], s_y[s][threadIdx.x], v);
     if (shared_w) {
       v += __bfloat162float(__float2bfloat16_rn(s_sh[threadIdx.x]));
     } else if (shared) {
