@@ -46,9 +46,14 @@
 // weight block, row block) so that CTAs running side by side share a weight
 // block in L2.
 //
+// Leading phase (weights-on-M, bf16): a launch may first compute one group of
+// up to 16 token rows with operands of its own (a shared expert), with its own
+// split plan and scratch; when those operands do not come from the previous
+// kernel it runs before the launch's wait on that kernel.
+//
 // Stream-K (weights-on-M form, every group <= 16 rows, scratch given; gate_up
-// and 8-bit launches): when
-// whole units do not spread evenly over the grid, the units' K blocks are laid
+// and 8-bit launches): when whole units do not spread evenly over the grid,
+// the units' K blocks are laid
 // end to end and every CTA takes an equal contiguous share.  A unit cut
 // between CTAs becomes pieces; each piece stores its fp32 partial accumulator
 // and takes a ticket on the unit's counter; the ticket holder that arrives
